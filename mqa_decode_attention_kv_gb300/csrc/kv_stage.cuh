@@ -1,0 +1,86 @@
+// One pipeline stage of int8 K/V: a 64-token tile fetched with TMA.
+//
+// Stage layout: K codes [64 rows][D] then V codes [64 rows][D], each written by
+// four 16-row TMA boxes with the 128-byte (D=128) or 64-byte (D=64) swizzle;
+// fp32 scales land in a separate [2][64] array (K then V).  A box is fetched
+// only if its 16 tokens overlap the key range [lo, L) and its block id is
+// inside the pool; bit c of *stage_mask records whether box c arrived.
+#pragma once
+
+#include "common.cuh"
+
+namespace mqa {
+
+template <int D>
+struct KvStage {
+    static constexpr int CODE_BYTES = kTileTokens * D;  // K (or V) codes of one tile
+    static constexpr int CODE_PAIR = 2 * CODE_BYTES;     // K then V
+    static constexpr uint32_t SWZ_MASK = (D == 128) ? 7u : 3u;
+};
+
+// Byte offset of (row, col) inside a K or V tile region written by TMA with
+// the swizzle of the code maps (the region base is 1024-byte aligned).
+template <int D>
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t col)
+{
+    const uint32_t o = row * D + col;
+    return o ^ (((o >> 7) & KvStage<D>::SWZ_MASK) << 4);
+}
+
+// Issue the copies of tile T (tokens [64T, 64T+64)) of one sequence into a
+// stage; called by a single thread.  `table` is the sequence's block-table row.
+template <int D>
+__device__ __forceinline__ void issue_kv_tile(const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                              const float *k_scale, const float *v_scale, const int32_t *table,
+                                              int num_blocks, int page_size, int32_t *dev_status,
+                                              uint8_t *codes_dst, float *scales_dst, uint64_t *bar,
+                                              uint32_t *stage_mask, int T, int lo, int L)
+{
+    uint8_t *kdst = codes_dst;
+    uint8_t *vdst = codes_dst + KvStage<D>::CODE_BYTES;
+    float *ksdst = scales_dst;
+    float *vsdst = scales_dst + kTileTokens;
+    int32_t rowbase[kChunksPerTile];
+    uint32_t mask = 0, bytes = 0;
+#pragma unroll
+    for (int c = 0; c < kChunksPerTile; ++c) {
+        const int t0 = T * kTileTokens + c * kChunkTokens;
+        rowbase[c] = -1;
+        if (t0 + kChunkTokens > lo && t0 < L) {
+            const int32_t blk = __ldg(table + t0 / page_size);
+            if (blk >= 0 && blk < num_blocks) {
+                rowbase[c] = blk * page_size + (t0 % page_size);
+                mask |= 1u << c;
+                bytes += 2 * kChunkTokens * D + 2 * kChunkTokens * 4;
+            } else {
+                set_status(dev_status, MQA_DEV_BAD_BLOCK);
+            }
+        }
+    }
+    *stage_mask = mask;
+    mbar_arrive_expect_tx(bar, bytes);
+    int run_c = -1, run_n = 0;
+#pragma unroll
+    for (int c = 0; c <= kChunksPerTile; ++c) {
+        const bool have = c < kChunksPerTile && rowbase[c] >= 0;
+        if (have) {
+            tma_load_2d(kdst + c * kChunkTokens * D, &k_map, 0, rowbase[c], bar);
+            tma_load_2d(vdst + c * kChunkTokens * D, &v_map, 0, rowbase[c], bar);
+        }
+        // scales: boxes whose slots are contiguous (same page) share one bulk copy
+        const bool extends = have && run_n > 0 && rowbase[c] == rowbase[run_c] + run_n * kChunkTokens;
+        if (!extends && run_n > 0) {
+            const uint32_t nb = run_n * kChunkTokens * 4;
+            bulk_load(ksdst + run_c * kChunkTokens, k_scale + rowbase[run_c], nb, bar);
+            bulk_load(vsdst + run_c * kChunkTokens, v_scale + rowbase[run_c], nb, bar);
+            run_n = 0;
+        }
+        if (have) {
+            if (run_n == 0)
+                run_c = c;
+            ++run_n;
+        }
+    }
+}
+
+}  // namespace mqa

@@ -1,0 +1,54 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mqa {
+
+struct AppendArgs {
+    int8_t *k_codes, *v_codes;
+    float *k_scale, *v_scale;
+    int32_t num_blocks, page_size, head_dim;
+    const int32_t *block_table, *seq_lens, *cu_new;
+    int32_t batch, max_blocks;
+    int32_t num_tokens;
+    const __nv_bfloat16 *k_new, *v_new;
+    int32_t *dev_status;
+};
+cudaError_t launch_quant_append(const AppendArgs &a, cudaStream_t s);
+
+struct DecodeArgs {
+    CUtensorMap k_map, v_map;          // 2-D maps over [num_blocks*page_size, head_dim] int8
+    const float *k_scale, *v_scale;
+    const int32_t *block_table, *seq_lens;
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;                // direct output (num_splits == 1)
+    float *o_partial, *lse;            // split output (num_splits > 1)
+    int32_t *dev_status;
+    int32_t batch, max_blocks, num_blocks, page_size, max_seq_len;
+    int32_t num_q_heads, window;
+    int32_t tiles_per_split, num_splits;
+    float q_scale_log2;                // sm_scale * log2(e)
+};
+cudaError_t launch_decode(const DecodeArgs &a, int head_dim, cudaStream_t s);
+int decode_ctas_per_sm(int head_dim, int num_q_heads);
+
+cudaError_t launch_combine(const float *o_partial, const float *lse, int32_t batch, int32_t num_splits,
+                           int32_t num_q_heads, int32_t head_dim, __nv_bfloat16 *out, cudaStream_t s);
+
+struct PrefillArgs {
+    CUtensorMap k_map, v_map;
+    const float *k_scale, *v_scale;
+    const int32_t *block_table, *seq_lens, *cu_q;
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    int32_t *dev_status;
+    int32_t batch, max_blocks, num_blocks, page_size, max_seq_len;
+    int32_t num_q_heads, window, total_q, max_q_len;
+    float q_scale_log2;
+};
+cudaError_t launch_prefill(const PrefillArgs &a, int head_dim, cudaStream_t s);
+
+}  // namespace mqa

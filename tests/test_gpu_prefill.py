@@ -1,0 +1,87 @@
+"""GPU parity of chunked causal prefill over prefix-shared int8 caches."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import mqa_decode_attention_kv_gb300 as mk
+from gpu_common import assert_close, caches_equal, sm_scale, to_dev_bf16, to_dev_i32
+
+pytestmark = pytest.mark.gpu
+
+
+def build_prefix_setup(rng, groups, per, prefix, new_counts, page, d, heads):
+    """Prefix blocks shared inside each group, written once through the group's
+    first sequence; then every sequence appends its own new tokens."""
+    new_counts = np.asarray(new_counts, np.int64)
+    max_new = int(new_counts.max())
+    pbs = synth.make_prefix_shared_batch(rng, groups, per, prefix, max_new, page)
+    B = groups * per
+    seq_lens = (prefix + new_counts).astype(np.int32)
+    gc = mk.KVCache.empty(pbs.num_blocks, page, d)
+    oc = oracle.Cache.empty(pbs.num_blocks, page, d)
+    # 1) shared prefixes
+    leaders = np.arange(groups) * per
+    lead_table = np.ascontiguousarray(pbs.block_table[leaders])
+    lead_lens = np.full(groups, prefix, np.int32)
+    cu_p = synth.cu_from_counts(lead_lens)
+    kp = synth.bf16_normal(rng, (int(cu_p[-1]), d))
+    vp = synth.bf16_normal(rng, (int(cu_p[-1]), d))
+    lead_batch = mk.Batch.from_host(lead_table, lead_lens)
+    mk.kv_quant_append(gc, lead_batch, to_dev_i32(cu_p), int(cu_p[-1]), to_dev_bf16(kp), to_dev_bf16(vp))
+    oracle.quant_append(oc, lead_table, lead_lens, cu_p, kp, vp)
+    # 2) new tokens of every sequence
+    batch = mk.Batch.from_host(pbs.block_table, seq_lens)
+    cu_q = synth.cu_from_counts(new_counts)
+    T = int(cu_q[-1])
+    kn = synth.bf16_normal(rng, (T, d))
+    vn = synth.bf16_normal(rng, (T, d))
+    cu_dev = to_dev_i32(cu_q)
+    mk.kv_quant_append(gc, batch, cu_dev, T, to_dev_bf16(kn), to_dev_bf16(vn))
+    oracle.quant_append(oc, pbs.block_table, seq_lens, cu_q, kn, vn)
+    q = synth.bf16_normal(rng, (T, heads, d))
+    torch.cuda.synchronize()
+    return dict(pbs=pbs, seq_lens=seq_lens, gc=gc, oc=oc, batch=batch, cu_q=cu_q, cu_dev=cu_dev, q=q,
+                max_new=max_new, d=d)
+
+
+def run(st, window, rows=None):
+    out = mk.mqa_prefill_attn([st["gc"]], [0], 0, window, st["batch"], st["cu_dev"], to_dev_bf16(st["q"]),
+                              st["max_new"], sm_scale=sm_scale(st["d"]))
+    torch.cuda.synchronize()
+    rs, rp = oracle.prefill_rows(st["cu_q"], st["seq_lens"])
+    if rows is not None:
+        rs, rp = rs[rows], rp[rows]
+    q = st["q"] if rows is None else np.ascontiguousarray(st["q"][rows])
+    ref, _ = oracle.attention(st["oc"], st["pbs"].block_table, st["seq_lens"], q, rs, rp, window,
+                              sm_scale(st["d"]))
+    got = out if rows is None else out[torch.from_numpy(rows).cuda()]
+    return got, ref
+
+
+@pytest.mark.parametrize("heads,d,page", [(32, 128, 64), (8, 64, 16), (16, 128, 16), (64, 128, 64)])
+def test_prefill_prefix_shared_ragged(heads, d, page):
+    rng = np.random.default_rng(heads + d + page)
+    counts = [100, 37, 64, 1, 129, 65]
+    st = build_prefix_setup(rng, 3, 2, 256, counts, page, d, heads)
+    assert caches_equal(st["gc"], st["oc"])
+    for window in (0, 1, 50, 300):
+        got, ref = run(st, window)
+        assert_close(got, ref, f"prefill H={heads} d={d} P={page} W={window}")
+
+
+def test_prefill_prefix_reuse_full_size_sampled():
+    """32 groups x 8 sequences sharing 8192-token prefixes, 512 new tokens each,
+    32 heads, d=128, page 64; local (1024) and global; sampled query rows."""
+    w = synth.CONFIGS["prefix_prefill"]
+    rng = np.random.default_rng(w.seed)
+    prefix, new = w.len_values
+    st = build_prefix_setup(rng, w.groups, w.batch // w.groups, prefix, [new] * w.batch, w.page_size,
+                            w.head_dim, w.num_q_heads)
+    T = int(st["cu_q"][-1])
+    rows = np.unique(np.concatenate([np.arange(0, new, 37), T - 1 - np.arange(0, new, 41),
+                                     synth.sample_rows(rng, T, 24)]))
+    for window in w.windows:
+        got, ref = run(st, window, rows)
+        assert_close(got, ref, f"prefix_prefill W={window}")
