@@ -1,0 +1,682 @@
+"""Benchmark of the int8 paged MQA serving hot path on one (or N replica) GPUs.
+
+Default workload (one "step"): a full decode step of a 24-layer local/global
+stack -- 20 local layers (window 1024) and 4 global layers, 12 caches shared by
+adjacent layers, batch 128, 32 query heads, d=128, context lengths lognormal
+(median 4096, cap 32768), int8 paged KV with page 64.  A step appends the new
+token of every sequence to each of the 12 caches (kv_quant_append) and runs
+the 24 decode-attention calls in layer order (split-KV + combine where the
+planner chooses it).  Other workloads (--workload) time a single local layer,
+a single long-context global layer, or the prefix-reuse chunked prefill.
+
+Prints ONE JSON line (rank 0).  See the design doc for the accounting and the
+meaning of every field.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from mqa_decode_attention_kv_gb300 import accounting as acc  # noqa: E402
+
+METRIC = "decode-attention KV GB/s (frac of HBM peak) and decode tokens/s on 1 GB300"
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+
+
+# ---------------------------------------------------------------- helpers
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def source_digest(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(name: str, digest: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/<name>,
+    used only if the kernel sources still match the digest recorded there."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 2 and not line.startswith("#"):
+            vals[parts[0]] = parts[1]
+    if vals.get("source_digest") != digest or "dram_bytes_per_launch" not in vals:
+        return None
+    return float(vals["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU workloads
+class DecodeStack:
+    """Caches, inputs and pre-marshalled C-ABI arguments of a decode step."""
+
+    def __init__(self, w: "synth.Workload", device):
+        import ctypes
+        import torch
+        import mqa_decode_attention_kv_gb300 as mk
+        self.w, self.mk, self.torch = w, mk, torch
+        rng = np.random.default_rng(w.seed)
+        self.lens = synth.seq_lens_for(w, rng)
+        self.pb = synth.make_paged_batch(rng, self.lens, w.page_size, shuffle=w.shuffle)
+        self.batch = mk.Batch.from_host(self.pb.block_table, self.lens, device=device)
+        B, H, D, P = w.batch, w.num_q_heads, w.head_dim, w.page_size
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1000 + w.seed)
+        T = int(self.lens.sum())
+        cu_all = torch.from_numpy(synth.cu_from_counts(self.lens)).to(device)
+        self.caches = []
+        for _ in range(w.num_caches):
+            c = mk.KVCache.empty(self.pb.num_blocks, P, D, device=device)
+            k = torch.randn((T, D), generator=gen, device=device).to(torch.bfloat16)
+            v = torch.randn((T, D), generator=gen, device=device).to(torch.bfloat16)
+            mk.kv_quant_append(c, self.batch, cu_all, T, k, v)
+            del k, v
+            self.caches.append(c)
+        L = w.num_layers
+        self.q = torch.randn((L, B, H, D), generator=gen, device=device).to(torch.bfloat16)
+        self.k_new = torch.randn((w.num_caches, B, D), generator=gen, device=device).to(torch.bfloat16)
+        self.v_new = torch.randn((w.num_caches, B, D), generator=gen, device=device).to(torch.bfloat16)
+        self.out = torch.empty_like(self.q)
+        self.cu_step = torch.arange(B + 1, dtype=torch.int32, device=device)
+        self.splits = [mk.mqa_decode_auto_splits(self.batch, w.windows[l], H, D, P) for l in range(L)]
+        ws = max(mk.mqa_decode_workspace_size(B, H, D, s) for s in self.splits)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        first = {}
+        for l, c in enumerate(w.layer_map):
+            first.setdefault(c, l)
+        self.append_before = {l: c for c, l in first.items()}  # layer -> cache appended just before it
+        # pre-marshalled arguments (same C ABI the binding uses, without per-call Python work)
+        self._carr = mk._caches_array(self.caches)
+        self._lmap = (ctypes.c_int32 * L)(*w.layer_map)
+        self._bt = self.batch.c()
+        self._cptr = [ctypes.byref(self._carr[i]) for i in range(len(self.caches))]
+        self.scale = 1.0 / math.sqrt(D)
+        self.lib = mk.lib()
+        self.bytes_per_layer = [acc.decode_kv_bytes(self.lens, w.windows[l], D) for l in range(L)]
+        self.flops_per_layer = [acc.decode_flops(self.lens, w.windows[l], H, D) for l in range(L)]
+
+    def launches_per_step(self) -> int:
+        return len(self.append_before) + sum(2 if s > 1 else 1 for s in self.splits)
+
+    def append(self, c: int, stream: int):
+        B = self.w.batch
+        rc = self.lib.kv_quant_append(self._cptr[c], self.torch_ptr_bt(), self.cu_step.data_ptr(), B,
+                                      self.k_new[c].data_ptr(), self.v_new[c].data_ptr(), None, stream)
+        assert rc == 0, rc
+
+    def torch_ptr_bt(self):
+        import ctypes
+        return ctypes.byref(self._bt)
+
+    def attend(self, l: int, stream: int):
+        import ctypes
+        w = self.w
+        rc = self.lib.mqa_decode_attn(self._carr, len(self.caches), self._lmap, w.num_layers, l, w.windows[l],
+                                      ctypes.byref(self._bt), self.q[l].data_ptr(), self.out[l].data_ptr(),
+                                      w.num_q_heads, self.scale, self.splits[l], self.ws.data_ptr(),
+                                      self.ws.numel(), None, stream)
+        assert rc == 0, rc
+
+    def step(self, stream: int):
+        for l in range(self.w.num_layers):
+            c = self.append_before.get(l)
+            if c is not None:
+                self.append(c, stream)
+            self.attend(l, stream)
+
+
+def flush_l2(buf):
+    """Evict L2 by reading a buffer larger than it (a read leaves no dirty lines
+    whose write-back would be charged to the next timed kernel)."""
+    buf.sum(dtype=torch_int64())
+
+
+def torch_int64():
+    import torch
+    return torch.int64
+
+
+def time_steps(fn, steps, flush_buf, stream):
+    """Per-step device time (ms) with CUDA events on `stream`, L2 flushed
+    before every step (outside the timed intervals)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush_l2(flush_buf)
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+    stream.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def cold_call_times(stack: DecodeStack, reps, flush_buf, stream):
+    """Device time of every attention call with L2 flushed before it: the
+    per-launch HBM roofline measurement.  Returns {layer: [ms, ...]}."""
+    import torch
+    sptr = stream.cuda_stream
+    res = {l: [] for l in range(stack.w.num_layers)}
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            for l in range(stack.w.num_layers):
+                c = stack.append_before.get(l)
+                if c is not None:
+                    stack.append(c, sptr)
+                flush_l2(flush_buf)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                stack.attend(l, sptr)
+                e1.record(stream)
+                evs.append((l, e0, e1))
+    stream.synchronize()
+    for l, e0, e1 in evs:
+        res[l].append(e0.elapsed_time(e1))
+    return res
+
+
+def e2e_steps(stack: DecodeStack, steps, stream):
+    """End-to-end step through the public Python API with host buffers: H2D of
+    the step's queries and new K/V from pinned memory, the appends and 24
+    attention calls, D2H of all outputs.  Returns (per-step ms, h2d, d2h bytes)."""
+    import torch
+    mk = stack.mk
+    w = stack.w
+    q_host = stack.q.cpu().pin_memory()
+    kn_host = stack.k_new.cpu().pin_memory()
+    vn_host = stack.v_new.cpu().pin_memory()
+    out_host = torch.empty(stack.out.shape, dtype=stack.out.dtype, pin_memory=True)
+    q_dev = torch.empty_like(stack.q)
+    kn_dev = torch.empty_like(stack.k_new)
+    vn_dev = torch.empty_like(stack.v_new)
+    out_dev = torch.empty_like(stack.out)
+    h2d = (q_host.numel() + kn_host.numel() + vn_host.numel()) * 2
+    d2h = out_host.numel() * 2
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            q_dev.copy_(q_host, non_blocking=True)
+            kn_dev.copy_(kn_host, non_blocking=True)
+            vn_dev.copy_(vn_host, non_blocking=True)
+            for l in range(w.num_layers):
+                c = stack.append_before.get(l)
+                if c is not None:
+                    mk.kv_quant_append(stack.caches[c], stack.batch, stack.cu_step, w.batch, kn_dev[c], vn_dev[c],
+                                       stream=stream)
+                mk.mqa_decode_attn(stack.caches, list(w.layer_map), l, w.windows[l], stack.batch, q_dev[l],
+                                   out=out_dev[l], num_splits=stack.splits[l], workspace=stack.ws, stream=stream)
+            out_host.copy_(out_dev, non_blocking=True)
+            e1.record(stream)
+            times.append((e0, e1))
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in times], h2d, d2h
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+def oracle_decode_sample(w: "synth.Workload", n_seqs: int, seed: int = 123):
+    """Time the oracle (single-threaded C, fp64) on a bounded sample of the
+    workload: n_seqs sequences drawn from the workload's length mix run through
+    every layer (append of the new token where a cache is first used, then
+    decode attention).  Returns (tokens/s, seconds, description)."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(w.seed)
+    lens_all = synth.seq_lens_for(w, rng)
+    pick = synth.sample_rows(np.random.default_rng(seed), len(lens_all), n_seqs)
+    lens = lens_all[pick]
+    pb = synth.make_paged_batch(rng, lens, w.page_size, shuffle=w.shuffle)
+    cu = synth.cu_from_counts(lens)
+    T = int(cu[-1])
+    d, H = w.head_dim, w.num_q_heads
+    caches = []
+    for _ in range(w.num_caches):
+        c = oracle.Cache.empty(pb.num_blocks, w.page_size, d)
+        oracle.quant_append(c, pb.block_table, lens, cu, synth.bf16_normal(rng, (T, d)),
+                            synth.bf16_normal(rng, (T, d)))
+        caches.append(c)
+    q = [synth.bf16_normal(rng, (len(lens), H, d)) for _ in range(w.num_layers)]
+    kn = [synth.bf16_normal(rng, (len(lens), d)) for _ in range(w.num_caches)]
+    vn = [synth.bf16_normal(rng, (len(lens), d)) for _ in range(w.num_caches)]
+    cu_step = synth.cu_from_counts(np.ones(len(lens)))
+    first = {}
+    for l, c in enumerate(w.layer_map):
+        first.setdefault(c, l)
+    before = {l: c for c, l in first.items()}
+    scale = 1.0 / math.sqrt(d)
+    t0 = time.perf_counter()
+    for l in range(w.num_layers):
+        c = before.get(l)
+        if c is not None:
+            oracle.quant_append(caches[c], pb.block_table, lens, cu_step, kn[c], vn[c])
+        oracle.decode(caches[w.layer_map[l]], pb.block_table, lens, q[l], w.windows[l], scale)
+    dt = time.perf_counter() - t0
+    desc = (f"{len(lens)} of {w.batch} sequences (seeded sample, mean context {lens.mean():.0f}) "
+            f"through all {w.num_layers} layers; one decode token each")
+    return len(lens) / dt, dt, desc
+
+
+class PrefillWorkload:
+    """Prefix-reuse chunked prefill: groups of sequences share int8 prefixes;
+    each sequence appends its new tokens (kv_quant_append over all of them) and
+    runs causal prefill attention over prefix + chunk, once with the local
+    window and once globally (two single-layer runs on the same cache)."""
+
+    def __init__(self, w: "synth.Workload", device):
+        import ctypes
+        import torch
+        import mqa_decode_attention_kv_gb300 as mk
+        self.w, self.mk = w, mk
+        rng = np.random.default_rng(w.seed)
+        prefix, new = w.len_values
+        per = w.batch // w.groups
+        pbs = synth.make_prefix_shared_batch(rng, w.groups, per, prefix, new, w.page_size)
+        self.lens = pbs.seq_lens
+        self.q_lens = np.full(w.batch, new, np.int64)
+        D, H = w.head_dim, w.num_q_heads
+        gen = torch.Generator(device=device)
+        gen.manual_seed(2000 + w.seed)
+        self.cache = mk.KVCache.empty(pbs.num_blocks, w.page_size, D, device=device)
+        leaders = np.arange(w.groups) * per
+        lead = mk.Batch.from_host(np.ascontiguousarray(pbs.block_table[leaders]),
+                                  np.full(w.groups, prefix, np.int32), device=device)
+        Tp = w.groups * prefix
+        cu_p = torch.from_numpy(synth.cu_from_counts([prefix] * w.groups)).to(device)
+        mk.kv_quant_append(self.cache, lead, cu_p, Tp,
+                           torch.randn((Tp, D), generator=gen, device=device).to(torch.bfloat16),
+                           torch.randn((Tp, D), generator=gen, device=device).to(torch.bfloat16))
+        self.batch = mk.Batch.from_host(pbs.block_table, self.lens, device=device)
+        self.T = w.batch * new
+        self.cu_q = torch.from_numpy(synth.cu_from_counts(self.q_lens)).to(device)
+        self.k_new = torch.randn((self.T, D), generator=gen, device=device).to(torch.bfloat16)
+        self.v_new = torch.randn((self.T, D), generator=gen, device=device).to(torch.bfloat16)
+        self.q = torch.randn((self.T, H, D), generator=gen, device=device).to(torch.bfloat16)
+        self.out = [torch.empty_like(self.q) for _ in w.windows]
+        self.max_q = new
+        self.lib = mk.lib()
+        self._c = self.cache.c()
+        self._carr = (mk._Cache * 1)(self._c)
+        self._lmap = (ctypes.c_int32 * len(w.windows))(*w.layer_map)
+        self._bt = self.batch.c()
+        self.scale = 1.0 / math.sqrt(D)
+        self.flops = [acc.prefill_flops(self.lens, self.q_lens, W, H, D) for W in w.windows]
+
+    def append(self, stream: int):
+        import ctypes
+        rc = self.lib.kv_quant_append(ctypes.byref(self._c), ctypes.byref(self._bt), self.cu_q.data_ptr(), self.T,
+                                      self.k_new.data_ptr(), self.v_new.data_ptr(), None, stream)
+        assert rc == 0, rc
+
+    def attend(self, l: int, stream: int):
+        import ctypes
+        w = self.w
+        rc = self.lib.mqa_prefill_attn(self._carr, 1, self._lmap, len(w.windows), l, w.windows[l],
+                                       ctypes.byref(self._bt), self.cu_q.data_ptr(), self.T, self.max_q,
+                                       self.q.data_ptr(), self.out[l].data_ptr(), w.num_q_heads, self.scale, None,
+                                       stream)
+        assert rc == 0, rc
+
+    def step(self, stream: int):
+        self.append(stream)
+        for l in range(len(self.w.windows)):
+            self.attend(l, stream)
+
+
+def dist_setup(world, local_rank):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def reduce_max(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- main
+def describe(w: "synth.Workload", lens) -> str:
+    if w.name == "prefix_prefill":
+        return (f"{w.name}: {w.groups} groups x {w.batch // w.groups} sequences sharing {w.len_values[0]}-token int8 "
+                f"prefixes (shared blocks), {w.len_values[1]} new tokens each; kv_quant_append of all new tokens, "
+                f"then causal MQA prefill with window {w.windows[0]} and global; {w.num_q_heads} q heads, "
+                f"d={w.head_dim}, page {w.page_size}")
+    n_glob = sum(1 for x in w.windows if x == 0)
+    return (f"{w.name}: {w.num_layers}-layer decode step ({w.num_layers - n_glob} local window "
+            f"{max(w.windows)} + {n_glob} global), {w.num_caches} caches via layer->cache map, batch {w.batch}, "
+            f"{w.num_q_heads} q heads, 1 int8 KV head, d={w.head_dim}, page {w.page_size}, "
+            f"ctx {w.len_kind} {w.len_values} (mean {float(np.mean(lens)):.0f})")
+
+
+def run_reference(args, w):
+    """Reference arm: the CPU oracle, as it stands, on the host cores."""
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    n = args.cpu_seqs
+    val, dt, desc = oracle_decode_sample(w, n)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": describe(w, synth.seq_lens_for(w, np.random.default_rng(w.seed)))},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_decode(args, w):
+    import torch
+    rank, world, local_rank = rank_info()
+    dist = dist_setup(world, local_rank)
+    device = f"cuda:{local_rank}"
+    torch.cuda.set_device(local_rank)
+    hbm, bf16, bf16_sus, peak_kind = measured_peaks()
+    stack = DecodeStack(w, device)
+    stream = torch.cuda.Stream(device=device)
+    sptr = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    B = w.batch
+    # eager warm-up, then capture the whole step in a CUDA graph
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            stack.step(sptr)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        stack.step(torch.cuda.current_stream().cuda_stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        times = time_steps(graph.replay, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    total_ms = reduce_max(dist, float(sum(times)))
+    ms = total_ms / args.steps
+    value = world * B * args.steps / (total_ms / 1000.0)
+    kv_bytes = sum(stack.bytes_per_layer)
+
+    # eager step (no graph) for reference
+    eager = time_steps(lambda: stack.step(sptr), max(3, min(args.steps, 10)), flush, stream)
+    # per-call cold-L2 timings: the roofline of the decode kernel (+ its split combine)
+    cold = cold_call_times(stack, args.roofline_reps, flush, stream)
+    cold_ms = {l: statistics.mean(v) for l, v in cold.items()}
+    achieved = sum(stack.bytes_per_layer) / (sum(cold_ms.values()) * 1e6)
+    loc = [l for l in range(w.num_layers) if w.windows[l] > 0]
+    glo = [l for l in range(w.num_layers) if w.windows[l] == 0]
+
+    def part(ls):
+        if not ls:
+            return None
+        t = sum(cold_ms[l] for l in ls)
+        return {"layers": len(ls), "ms_per_call": t / len(ls),
+                "gbps": sum(stack.bytes_per_layer[l] for l in ls) / (t * 1e6),
+                "splits": sorted(set(stack.splits[l] for l in ls))}
+
+    digest = source_digest(["mqa_decode_attention_kv_gb300/csrc/decode.cu",
+                            "mqa_decode_attention_kv_gb300/csrc/kv_stage.cuh",
+                            "mqa_decode_attention_kv_gb300/csrc/common.cuh"])
+    traffic = profile_traffic(f"decode_{w.name}_traffic.txt", digest)
+    e2e = None
+    if not args.no_e2e:
+        et, h2d, d2h = e2e_steps(stack, max(3, min(args.steps, 10)), stream)
+        e2e = {"value": world * B / (statistics.mean(et) / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(et)}
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        val, dt, desc = oracle_decode_sample(w, args.cpu_seqs)
+        cpu = {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc, "seconds": dt}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "i8kv-f16mma-f32acc", "data": "synthetic",
+        "config": {"workload": describe(w, stack.lens), "global_batch": B * world,
+                   "seq_len": f"{w.len_kind} {w.len_values}", "parallelism": f"replicas x{world}",
+                   "l2": "L2 flushed (512 MB read) before every timed step; inputs (KV read per step) exceed L2",
+                   "timing": "CUDA graph of the whole step, replayed; CUDA events on the launching stream",
+                   "kv_bytes_per_step": kv_bytes, "kv_gbps": kv_bytes / (ms * 1e6)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "decode attention call (decode kernel + split-KV combine), each call timed "
+                               "alone with L2 flushed before it",
+                     "local": part(loc), "global": part(glo)},
+        "eager_ms_per_step": statistics.mean(eager),
+        "gpu_launches": stack.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def run_prefill(args, w):
+    import torch
+    rank, world, local_rank = rank_info()
+    dist = dist_setup(world, local_rank)
+    device = f"cuda:{local_rank}"
+    torch.cuda.set_device(local_rank)
+    hbm, bf16, bf16_sus, peak_kind = measured_peaks()
+    wl = PrefillWorkload(w, device)
+    stream = torch.cuda.Stream(device=device)
+    sptr = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            wl.step(sptr)
+    stream.synchronize()
+    barrier(dist)
+    with ClockSampler(local_rank) as clk:
+        times = time_steps(lambda: wl.step(sptr), args.steps, flush, stream)
+    barrier(dist)
+    total_ms = reduce_max(dist, float(sum(times)))
+    ms = total_ms / args.steps
+    flops = sum(wl.flops)
+    value = world * flops / (ms * 1e-3) / 1e12
+    # per-call timing of the prefill kernel (the dominant kernel) and of the append
+    per = {l: [] for l in range(len(w.windows))}
+    app = []
+    with torch.cuda.stream(stream):
+        evs = []
+        for _ in range(args.roofline_reps):
+            flush_l2(flush)
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            wl.append(sptr)
+            a1.record(stream)
+            for l in range(len(w.windows)):
+                flush_l2(flush)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                wl.attend(l, sptr)
+                e1.record(stream)
+                evs.append((l, e0, e1))
+            app.append((a0, a1))
+    stream.synchronize()
+    for l, e0, e1 in evs:
+        per[l].append(e0.elapsed_time(e1))
+    per_ms = [statistics.mean(per[l]) for l in range(len(w.windows))]
+    app_ms = statistics.mean(a.elapsed_time(b) for a, b in app)
+    achieved = sum(wl.flops) / (sum(per_ms) * 1e-3) / 1e12
+    append_bytes = wl.T * w.head_dim * 2 * 2 + wl.T * (2 * w.head_dim + 8)
+    if rank != 0:
+        return
+    line = {
+        "metric": "prefix-reuse chunked prefill attention TFLOP/s on 1 GB300", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "i8kv-f16mma-f32acc", "data": "synthetic",
+        "config": {"workload": describe(w, wl.lens), "global_batch": w.batch * world,
+                   "parallelism": f"replicas x{world}", "l2": "L2 flushed (512 MB read) before every timed step and call",
+                   "prefill_flops_per_step": flops, "tokens_per_step": wl.T},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": achieved / bf16, "traffic": None,
+                     "peak_source": f"{peak_kind} bf16_tflops (fp16 dense rate = bf16 rate)",
+                     "kernel": "mqa_prefill_attn kernel, each call timed alone",
+                     "ms_per_call": dict(zip([f"window_{x}" for x in w.windows], per_ms))},
+        "append": {"ms": app_ms, "gbps": append_bytes / (app_ms * 1e6), "tokens": wl.T},
+        "gpu_launches": (1 + len(w.windows)) * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_profile(args, w):
+    """Set-up plus a few eager steps, nothing else: a short, bounded program
+    for ncu (one GPU)."""
+    import torch
+    torch.cuda.set_device(0)
+    wl = PrefillWorkload(w, "cuda:0") if w.name == "prefix_prefill" else DecodeStack(w, "cuda:0")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            wl.step(stream.cuda_stream)
+    stream.synchronize()
+    print(f"profile run done: {args.steps} steps of {w.name}", flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="stack24_b128", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--roofline-reps", type=int, default=3)
+    ap.add_argument("--cpu-seqs", type=int, default=32, help="sequences in the oracle's timed sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="set up the workload, run --steps eager steps and exit (for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.profile:
+        ap.error("--warmup must be >= 3")
+    w = synth.CONFIGS[args.workload]
+    if args.impl == "reference":
+        if w.name == "prefix_prefill":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle baseline covers decode workloads only"}))
+            return
+        run_reference(args, w)
+        return
+    from mqa_decode_attention_kv_gb300 import build as _b
+    _b.build()
+    if args.profile:
+        run_profile(args, w)
+    elif w.name == "prefix_prefill":
+        run_prefill(args, w)
+    else:
+        run_decode(args, w)
+
+
+if __name__ == "__main__":
+    main()

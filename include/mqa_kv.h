@@ -119,7 +119,7 @@ int kv_quant_append(const mqa_kv_cache *cache, const mqa_batch *batch, const int
  * the tiled online softmax of the workshop transcript, 00:47:59-00:49:13.
  *
  *   caches[num_caches], layer_to_kv[num_layers]: HOST arrays.
- *   q:   bf16 [batch][num_q_heads][head_dim], 16-byte aligned.
+ *   q:   bf16 [batch][num_q_heads][head_dim], 16-byte aligned.  sm_scale > 0.
  *   out: bf16 [batch][num_q_heads][head_dim], 16-byte aligned.
  *   num_splits: 0 = choose automatically (see mqa_decode_auto_splits), 1 = one
  *        CTA per sequence, S > 1 = up to S key ranges per sequence processed in

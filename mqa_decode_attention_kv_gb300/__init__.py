@@ -55,6 +55,27 @@ class _Batch(ctypes.Structure):
 _lib_handle = None
 
 
+def declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Set the argument and return types of every entry point on a loaded
+    libmqa_kv handle (64-bit pointers must never pass as default C ints)."""
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    L.kv_quant_append.argtypes = [P, P, P, i32, P, P, P, P]
+    L.kv_quant_append.restype = ctypes.c_int
+    L.mqa_decode_attn.argtypes = [P, i32, P, i32, i32, i32, P, P, P, i32, ctypes.c_float, i32, P, sz, P, P]
+    L.mqa_decode_attn.restype = ctypes.c_int
+    L.mqa_decode_auto_splits.argtypes = [P, i32, i32, i32, i32]
+    L.mqa_decode_auto_splits.restype = ctypes.c_int
+    L.mqa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.mqa_decode_workspace_size.restype = sz
+    L.split_kv_combine.argtypes = [P, P, i32, i32, i32, i32, P, P]
+    L.split_kv_combine.restype = ctypes.c_int
+    L.mqa_prefill_attn.argtypes = [P, i32, P, i32, i32, i32, P, P, i32, i32, P, P, i32, ctypes.c_float, P, P]
+    L.mqa_prefill_attn.restype = ctypes.c_int
+    L.mqa_status_str.argtypes = [ctypes.c_int]
+    L.mqa_status_str.restype = ctypes.c_char_p
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """Load libmqa_kv.so (raises if it has not been built)."""
     global _lib_handle
@@ -62,23 +83,7 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                                "`python -m mqa_decode_attention_kv_gb300.build`")
-        L = ctypes.CDLL(LIB_PATH)
-        P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
-        L.kv_quant_append.argtypes = [P, P, P, i32, P, P, P, P]
-        L.kv_quant_append.restype = ctypes.c_int
-        L.mqa_decode_attn.argtypes = [P, i32, P, i32, i32, i32, P, P, P, i32, ctypes.c_float, i32, P, sz, P, P]
-        L.mqa_decode_attn.restype = ctypes.c_int
-        L.mqa_decode_auto_splits.argtypes = [P, i32, i32, i32, i32]
-        L.mqa_decode_auto_splits.restype = ctypes.c_int
-        L.mqa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
-        L.mqa_decode_workspace_size.restype = sz
-        L.split_kv_combine.argtypes = [P, P, i32, i32, i32, i32, P, P]
-        L.split_kv_combine.restype = ctypes.c_int
-        L.mqa_prefill_attn.argtypes = [P, i32, P, i32, i32, i32, P, P, i32, i32, P, P, i32, ctypes.c_float, P, P]
-        L.mqa_prefill_attn.restype = ctypes.c_int
-        L.mqa_status_str.argtypes = [ctypes.c_int]
-        L.mqa_status_str.restype = ctypes.c_char_p
-        _lib_handle = L
+        _lib_handle = declare(ctypes.CDLL(LIB_PATH))
     return _lib_handle
 
 

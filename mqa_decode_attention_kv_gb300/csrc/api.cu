@@ -306,7 +306,7 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
         return rc;
     if (!heads_ok(num_q_heads))
         return MQA_ERR_UNSUPPORTED;
-    if (window < 0 || num_splits < 0 || num_splits > MQA_MAX_SPLITS || !std::isfinite(sm_scale))
+    if (window < 0 || num_splits < 0 || num_splits > MQA_MAX_SPLITS || !(std::isfinite(sm_scale) && sm_scale > 0.f))
         return MQA_ERR_INVALID_ARG;
     rc = check_batch(batch, cache->page_size);
     if (rc != MQA_OK)
@@ -388,7 +388,7 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
         return rc;
     if (!heads_ok(num_q_heads))
         return MQA_ERR_UNSUPPORTED;
-    if (window < 0 || total_q < 0 || max_q_len < 0 || !std::isfinite(sm_scale))
+    if (window < 0 || total_q < 0 || max_q_len < 0 || !(std::isfinite(sm_scale) && sm_scale > 0.f))
         return MQA_ERR_INVALID_ARG;
     rc = check_batch(batch, cache->page_size);
     if (rc != MQA_OK)

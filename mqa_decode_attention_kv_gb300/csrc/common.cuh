@@ -9,7 +9,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/mqa_kv.h"
+#include "mqa_kv.h"
 
 namespace mqa {
 
@@ -18,6 +18,7 @@ constexpr int kTileTokens = 64;   // tokens per pipeline stage
 constexpr int kChunkTokens = 16;  // rows per TMA box (a box never crosses a page: P in {16, 64})
 constexpr int kChunksPerTile = kTileTokens / kChunkTokens;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
+constexpr uint32_t kTryWaitSuspendNs = 1000000;  // let a waiting thread sleep instead of spinning
 
 // ---------------------------------------------------------------- addressing
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -51,6 +52,13 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
@@ -62,10 +70,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kTryWaitSuspendNs)
         : "memory");
     return ok != 0;
 }

@@ -11,6 +11,8 @@
 
 namespace mqa {
 
+constexpr int32_t kNoBlock = INT32_MIN;  // "box not needed" (never a table entry we accept)
+
 template <int D>
 struct KvStage {
     static constexpr int CODE_BYTES = kTileTokens * D;  // K (or V) codes of one tile
@@ -27,14 +29,28 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t col)
     return o ^ (((o >> 7) & KvStage<D>::SWZ_MASK) << 4);
 }
 
-// Issue the copies of tile T (tokens [64T, 64T+64)) of one sequence into a
-// stage; called by a single thread.  `table` is the sequence's block-table row.
+// Physical block ids of the four 16-token boxes of tile T (tokens [64T, 64T+64)):
+// kNoBlock for a box outside the key range [lo, L).  The loads are independent, so a
+// caller can issue them a tile ahead of use.
+__device__ __forceinline__ void fetch_tile_blocks(const int32_t *table, int page_size, int T, int lo, int L,
+                                                  int32_t (&ids)[kChunksPerTile])
+{
+#pragma unroll
+    for (int c = 0; c < kChunksPerTile; ++c) {
+        const int t0 = T * kTileTokens + c * kChunkTokens;
+        ids[c] = (t0 + kChunkTokens > lo && t0 < L) ? __ldg(table + t0 / page_size) : kNoBlock;
+    }
+}
+
+// Issue the copies of tile T into a stage from block ids fetched by
+// fetch_tile_blocks (kNoBlock = not needed); called by a single thread.  Ids outside
+// the pool are reported in dev_status and their boxes skipped.
 template <int D>
-__device__ __forceinline__ void issue_kv_tile(const CUtensorMap &k_map, const CUtensorMap &v_map,
-                                              const float *k_scale, const float *v_scale, const int32_t *table,
-                                              int num_blocks, int page_size, int32_t *dev_status,
-                                              uint8_t *codes_dst, float *scales_dst, uint64_t *bar,
-                                              uint32_t *stage_mask, int T, int lo, int L)
+__device__ __forceinline__ void issue_kv_tile_ids(const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                                  const float *k_scale, const float *v_scale,
+                                                  const int32_t (&ids)[kChunksPerTile], int num_blocks,
+                                                  int page_size, int32_t *dev_status, uint8_t *codes_dst,
+                                                  float *scales_dst, uint64_t *bar, uint32_t *stage_mask, int T)
 {
     uint8_t *kdst = codes_dst;
     uint8_t *vdst = codes_dst + KvStage<D>::CODE_BYTES;
@@ -46,15 +62,12 @@ __device__ __forceinline__ void issue_kv_tile(const CUtensorMap &k_map, const CU
     for (int c = 0; c < kChunksPerTile; ++c) {
         const int t0 = T * kTileTokens + c * kChunkTokens;
         rowbase[c] = -1;
-        if (t0 + kChunkTokens > lo && t0 < L) {
-            const int32_t blk = __ldg(table + t0 / page_size);
-            if (blk >= 0 && blk < num_blocks) {
-                rowbase[c] = blk * page_size + (t0 % page_size);
-                mask |= 1u << c;
-                bytes += 2 * kChunkTokens * D + 2 * kChunkTokens * 4;
-            } else {
-                set_status(dev_status, MQA_DEV_BAD_BLOCK);
-            }
+        if (ids[c] >= 0 && ids[c] < num_blocks) {
+            rowbase[c] = ids[c] * page_size + (t0 % page_size);
+            mask |= 1u << c;
+            bytes += 2 * kChunkTokens * D + 2 * kChunkTokens * 4;
+        } else if (ids[c] != kNoBlock) {
+            set_status(dev_status, MQA_DEV_BAD_BLOCK);
         }
     }
     *stage_mask = mask;
@@ -81,6 +94,56 @@ __device__ __forceinline__ void issue_kv_tile(const CUtensorMap &k_map, const CU
             ++run_n;
         }
     }
+}
+
+// fetch + issue in one step (block-table latency not hidden)
+template <int D>
+__device__ __forceinline__ void issue_kv_tile(const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                              const float *k_scale, const float *v_scale, const int32_t *table,
+                                              int num_blocks, int page_size, int32_t *dev_status,
+                                              uint8_t *codes_dst, float *scales_dst, uint64_t *bar,
+                                              uint32_t *stage_mask, int T, int lo, int L)
+{
+    int32_t ids[kChunksPerTile];
+    fetch_tile_blocks(table, page_size, T, lo, L, ids);
+    issue_kv_tile_ids<D>(k_map, v_map, k_scale, v_scale, ids, num_blocks, page_size, dev_status, codes_dst,
+                         scales_dst, bar, stage_mask, T);
+}
+
+
+// One warp's share of a tile: box c (16 tokens) of tile T, issued by the warp's
+// lane 0 from a block id fetched earlier (kNoBlock = not needed).  Arrives once
+// on `bar` (initialised for kChunksPerTile arrivals) with the box's transaction
+// bytes, and records in *box_ok whether the box is coming.
+template <int D>
+__device__ __forceinline__ void issue_kv_box(const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                             const float *k_scale, const float *v_scale, int32_t id,
+                                             int num_blocks, int page_size, int32_t *dev_status,
+                                             uint8_t *codes_dst, float *scales_dst, uint64_t *bar,
+                                             uint32_t *box_ok, int T, int c)
+{
+    const int t0 = T * kTileTokens + c * kChunkTokens;
+    const bool ok = id >= 0 && id < num_blocks;
+    if (!ok && id != kNoBlock)
+        set_status(dev_status, MQA_DEV_BAD_BLOCK);
+    *box_ok = ok ? 1u : 0u;
+    if (!ok) {
+        mbar_arrive_expect_tx(bar, 0);
+        return;
+    }
+    const int row = id * page_size + (t0 % page_size);
+    mbar_arrive_expect_tx(bar, 2 * kChunkTokens * D + 2 * kChunkTokens * 4);
+    tma_load_2d(codes_dst + c * kChunkTokens * D, &k_map, 0, row, bar);
+    tma_load_2d(codes_dst + KvStage<D>::CODE_BYTES + c * kChunkTokens * D, &v_map, 0, row, bar);
+    bulk_load(scales_dst + c * kChunkTokens, k_scale + row, kChunkTokens * 4, bar);
+    bulk_load(scales_dst + kTileTokens + c * kChunkTokens, v_scale + row, kChunkTokens * 4, bar);
+}
+
+// Block id of box c of tile T (kNoBlock when the box lies outside [lo, L)).
+__device__ __forceinline__ int32_t fetch_box_block(const int32_t *table, int page_size, int T, int c, int lo, int L)
+{
+    const int t0 = T * kTileTokens + c * kChunkTokens;
+    return (t0 + kChunkTokens > lo && t0 < L) ? __ldg(table + t0 / page_size) : kNoBlock;
 }
 
 }  // namespace mqa

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         orow[hf] = ((size_t)(q0 + t) * H + h) * D;
     }
     {
-        // query fragments: natural k order, scaled by sm_scale*log2(e)*2^e per row
+        // query fragments: natural k order, scaled by 2^e per row (exact in fp16)
         uint32_t w[2][D / 2];
         float amax[2];
 #pragma unroll
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-            const float sm = amax[hf] * a.q_scale_log2;
+            const float sm = amax[hf];
             int e = 0;
             if (sm > 0.f && isfinite(sm)) {
                 int x;
@@ -162,8 +162,8 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
                 e = 14 - x;
                 e = e < -120 ? -120 : (e > 120 ? 120 : e);
             }
-            gexp[hf] = exp2i(-e);
-            const float f = a.q_scale_log2 * exp2i(e);
+            gexp[hf] = a.q_scale_log2 * exp2i(-e);  // q * 2^e is exact in fp16
+            const float f = exp2i(e);
 #pragma unroll
             for (int kt = 0; kt < C::KSTEPS; ++kt) {
                 const uint32_t lo32 = w[hf][2 * kt], hi32 = w[hf][2 * kt + 1];
