@@ -13,7 +13,7 @@ using namespace mqa;
 
 namespace {
 
-constexpr int kMinTilesPerSplit = 2;
+constexpr int kMinTilesPerSplit = 2;  // below this a split's fixed costs dominate
 
 bool aligned16(const void *p)
 {
@@ -182,17 +182,30 @@ int plan_decode(const mqa_batch *bt, int window, int heads, int head_dim, int re
     }
     int splits = requested;
     if (splits == 0) {
+        // the most splits whose CTAs still fit in one wave of resident CTAs
+        // (a second, partial wave would pay every CTA's start-up latency twice)
         const int sms = sm_count();
         if (sms <= 0)
             return MQA_ERR_CUDA;
         const int groups = (heads + 31) / 32;
-        const long long target = (long long)sms * ctas_per_sm(head_dim, heads);
-        long long tps = (total * groups + target - 1) / target;
-        if (tps < kMinTilesPerSplit)
-            tps = kMinTilesPerSplit;
-        splits = (int)((max_tiles + tps - 1) / tps);
-        if ((long long)bt->batch * groups >= target)
-            splits = 1;
+        const long long slots = (long long)sms * ctas_per_sm(head_dim, heads);
+        splits = 1;
+        for (int s = 2; s <= max_tiles && s <= MQA_MAX_SPLITS; ++s) {
+            const int tps = (max_tiles + s - 1) / s;
+            if (tps < kMinTilesPerSplit)
+                break;
+            long long ctas = 0;
+            if (bt->seq_lens_host != nullptr) {
+                for (int b = 0; b < bt->batch; ++b)
+                    ctas += (tiles_for(bt->seq_lens_host[b], window) + tps - 1) / tps;
+            } else {
+                ctas = (long long)bt->batch * ((max_tiles + tps - 1) / tps);
+            }
+            ctas *= groups;
+            if (ctas > slots)
+                break;
+            splits = s;
+        }
     }
     if (splits < 1)
         splits = 1;
