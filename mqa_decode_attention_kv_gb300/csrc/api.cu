@@ -219,11 +219,19 @@ int plan_decode(const mqa_batch *bt, int window, int heads, int head_dim, int re
     return MQA_OK;
 }
 
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
 size_t lse_offset(int32_t batch, int32_t heads, int32_t head_dim, int32_t splits)
 {
-    const size_t o = (size_t)batch * splits * heads * head_dim * sizeof(float);
-    return (o + 255) & ~size_t(255);
+    return round256((size_t)batch * splits * heads * head_dim * sizeof(float));
 }
+
+size_t counters_offset(int32_t batch, int32_t heads, int32_t head_dim, int32_t splits)
+{
+    return round256(lse_offset(batch, heads, head_dim, splits) + (size_t)batch * splits * heads * sizeof(float));
+}
+
+int head_groups(int32_t heads) { return (heads + 31) / 32; }
 
 }  // namespace
 
@@ -288,7 +296,8 @@ size_t mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t hea
 {
     if (num_splits <= 1 || batch <= 0 || num_q_heads <= 0 || head_dim <= 0)
         return 0;
-    return lse_offset(batch, num_q_heads, head_dim, num_splits) + (size_t)batch * num_splits * num_q_heads * 4;
+    return counters_offset(batch, num_q_heads, head_dim, num_splits) +
+           (size_t)batch * head_groups(num_q_heads) * sizeof(int32_t);
 }
 
 int mqa_decode_auto_splits(const mqa_batch *batch, int32_t window, int32_t num_q_heads, int32_t head_dim,
@@ -342,6 +351,9 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
         a.o_partial = static_cast<float *>(workspace);
         a.lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                           lse_offset(batch->batch, num_q_heads, D, plan.num_splits));
+        if (plan.num_splits <= kMaxFusedSplits)
+            a.counters = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                                     counters_offset(batch->batch, num_q_heads, D, plan.num_splits));
     }
     if ((rc = make_code_map(&a.k_map, cache->k_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
         return rc;
@@ -365,9 +377,15 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
     a.num_splits = plan.num_splits;
     a.q_scale_log2 = sm_scale * 1.4426950408889634f;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // up to kMaxFusedSplits splits the decode kernel merges them itself (its
+    // tickets start at zero); wider splits go through the combine kernel
+    if (a.counters != nullptr &&
+        cudaMemsetAsync(a.counters, 0, (size_t)a.batch * head_groups(num_q_heads) * sizeof(int32_t), s) !=
+            cudaSuccess)
+        return MQA_ERR_CUDA;
     if (launch_decode(a, D, s) != cudaSuccess)
         return MQA_ERR_CUDA;
-    if (plan.num_splits > 1 &&
+    if (plan.num_splits > 1 && a.counters == nullptr &&
         launch_combine(a.o_partial, a.lse, a.batch, a.num_splits, num_q_heads, D, a.out, s) != cudaSuccess)
         return MQA_ERR_CUDA;
     return MQA_OK;

@@ -26,6 +26,7 @@ struct DecodeArgs {
     const __nv_bfloat16 *q;
     __nv_bfloat16 *out;                // direct output (num_splits == 1)
     float *o_partial, *lse;            // split output (num_splits > 1)
+    int32_t *counters;                 // [batch][head groups] zeroed tickets: fused merge, or null
     int32_t *dev_status;
     int32_t batch, max_blocks, num_blocks, page_size, max_seq_len;
     int32_t num_q_heads, window;
@@ -34,6 +35,7 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs &a, int head_dim, cudaStream_t s);
 int decode_ctas_per_sm(int head_dim, int num_q_heads);
+constexpr int kMaxFusedSplits = 16;  // the decode kernel merges up to this many splits itself
 
 cudaError_t launch_combine(const float *o_partial, const float *lse, int32_t batch, int32_t num_splits,
                            int32_t num_q_heads, int32_t head_dim, __nv_bfloat16 *out, cudaStream_t s);

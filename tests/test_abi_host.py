@@ -48,8 +48,11 @@ def test_status_strings(L):
 def test_workspace_size_formula(L):
     assert mk.mqa_decode_workspace_size(8, 32, 128, 1) == 0
     n = mk.mqa_decode_workspace_size(8, 32, 128, 10)
-    part = 8 * 10 * 32 * 128 * 4
-    assert n == ((part + 255) // 256) * 256 + 8 * 10 * 32 * 4
+    r256 = lambda x: (x + 255) // 256 * 256
+    part = 8 * 10 * 32 * 128 * 4           # fp32 partial outputs
+    lse = 8 * 10 * 32 * 4                  # fp32 log-sum-exps
+    tickets = 8 * 1 * 4                    # one int32 per (sequence, group of 32 heads)
+    assert n == r256(r256(part) + lse) + tickets
 
 
 def cache(num_blocks=16, page=16, d=64, **kw):
