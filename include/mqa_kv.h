@@ -178,6 +178,27 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
                      const int32_t *cu_q, int32_t total_q, int32_t max_q_len, const void *q, void *out,
                      int32_t num_q_heads, float sm_scale, int32_t *dev_status, void *stream);
 
+/* Decode attention without a workspace argument, for callers that cannot
+ * allocate device memory (for example code running while a framework captures
+ * a CUDA graph and forbids new allocations, serving loops whose memory budget
+ * is reserved up front, or plugins with no access to the process's allocator).
+ * The paper has no counterpart to this call; it exists for those callers.
+ *
+ * Same arguments and results as mqa_decode_attn, minus workspace.  Split-KV
+ * partials go to one library-owned device array of 32 MiB that every GPU which
+ * loads the library holds until the process exits.  num_splits == 0 picks the
+ * automatic plan, narrowed until its workspace fits 32 MiB; an explicit
+ * num_splits whose workspace exceeds 32 MiB returns MQA_ERR_WORKSPACE.  The
+ * call allocates nothing (no cudaMalloc, no library allocation).  Every call
+ * shares the one array: calls whose GPU work overlaps (other streams, other
+ * threads) race and must be serialised by the caller.  The first call on a
+ * device looks up the array's device address; make that first call before any
+ * stream capture. */
+int mqa_decode_attn_noalloc(const mqa_kv_cache *caches, int32_t num_caches, const int32_t *layer_to_kv,
+                            int32_t num_layers, int32_t layer, int32_t window, const mqa_batch *batch,
+                            const void *q, void *out, int32_t num_q_heads, float sm_scale, int32_t num_splits,
+                            int32_t *dev_status, void *stream);
+
 /* A static, human-readable name for a return code. */
 const char *mqa_status_str(int status);
 

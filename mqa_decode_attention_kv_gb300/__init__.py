@@ -30,7 +30,7 @@ MQA_DEV_TIMEOUT = 8
 MQA_MAX_SPLITS = 1024
 
 EXPORTED = ("kv_quant_append", "mqa_decode_attn", "mqa_decode_auto_splits", "mqa_decode_workspace_size",
-            "split_kv_combine", "mqa_prefill_attn", "mqa_status_str")
+            "split_kv_combine", "mqa_prefill_attn", "mqa_status_str", "mqa_decode_attn_noalloc")
 
 
 class MQAError(RuntimeError):
@@ -71,6 +71,8 @@ def declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.split_kv_combine.restype = ctypes.c_int
     L.mqa_prefill_attn.argtypes = [P, i32, P, i32, i32, i32, P, P, i32, i32, P, P, i32, ctypes.c_float, P, P]
     L.mqa_prefill_attn.restype = ctypes.c_int
+    L.mqa_decode_attn_noalloc.argtypes = [P, i32, P, i32, i32, i32, P, P, P, i32, ctypes.c_float, i32, P, P]
+    L.mqa_decode_attn_noalloc.restype = ctypes.c_int
     L.mqa_status_str.argtypes = [ctypes.c_int]
     L.mqa_status_str.restype = ctypes.c_char_p
     return L
