@@ -34,6 +34,10 @@ struct DecodeArgs {
     float q_scale_log2;                // sm_scale * log2(e)
 };
 cudaError_t launch_decode(const DecodeArgs &a, int head_dim, cudaStream_t s);
+// head_dim 128 with 32 or 64 query heads runs on the tcgen05 kernel; the rest on the warp-MMA kernel
+inline bool decode_uses_tc(int head_dim, int num_q_heads) { return head_dim == 128 && num_q_heads >= 32; }
+cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s);
+int decode_tc_ctas_per_sm();
 int decode_ctas_per_sm(int head_dim, int num_q_heads);
 constexpr int kMaxFusedSplits = 16;  // the decode kernel merges up to this many splits itself
 
