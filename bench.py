@@ -169,6 +169,8 @@ class DecodeStack:
         self.splits = [mk.mqa_decode_auto_splits(self.batch, w.windows[l], H, D, P) for l in range(L)]
         ws = max(mk.mqa_decode_workspace_size(B, H, D, s) for s in self.splits)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        # device-side error bits of every call (bad inputs, a bounded wait that ran out)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
         first = {}
         for l, c in enumerate(w.layer_map):
             first.setdefault(c, l)
@@ -202,7 +204,7 @@ class DecodeStack:
         rc = self.lib.mqa_decode_attn(self._carr, len(self.caches), self._lmap, w.num_layers, l, w.windows[l],
                                       ctypes.byref(self._bt), self.q[l].data_ptr(), self.out[l].data_ptr(),
                                       w.num_q_heads, self.scale, self.splits[l], self.ws.data_ptr(),
-                                      self.ws.numel(), None, stream)
+                                      self.ws.numel(), ctypes.c_void_p(self.status.data_ptr()), stream)
         assert rc == 0, rc
 
     def step(self, stream: int):
@@ -521,7 +523,8 @@ def run_decode(args, w):
                 "gbps": sum(stack.bytes_per_layer[l] for l in ls) / (t * 1e6),
                 "splits": sorted(set(stack.splits[l] for l in ls))}
 
-    digest = source_digest(["mqa_decode_attention_kv_gb300/csrc/decode.cu",
+    digest = source_digest(["mqa_decode_attention_kv_gb300/csrc/decode_tc.cu",
+                            "mqa_decode_attention_kv_gb300/csrc/decode.cu",
                             "mqa_decode_attention_kv_gb300/csrc/kv_stage.cuh",
                             "mqa_decode_attention_kv_gb300/csrc/common.cuh"])
     traffic = profile_traffic(f"decode_{w.name}_traffic.txt", digest)
@@ -547,8 +550,8 @@ def run_decode(args, w):
                    "kv_bytes_per_step": kv_bytes, "kv_gbps": kv_bytes / (ms * 1e6)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "decode attention call (decode kernel; split-KV merge fused for <= 16 splits, "
-                               "else followed by the combine kernel), each call timed alone with L2 flushed before it",
+                     "kernel": "decode attention call (memset of the merge tickets + the decode kernel, split "
+                               "merge fused), each call timed alone with L2 flushed before it",
                      "local": part(loc), "global": part(glo)},
         "eager_ms_per_step": statistics.mean(eager),
         "gpu_launches": stack.launches_per_step() * args.steps,
@@ -558,7 +561,13 @@ def run_decode(args, w):
         line["e2e"] = e2e
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    dev_status = int(stack.status.item())
+    if dev_status:
+        # a call flagged bad input or a wait that ran out: the timings are not valid
+        line["device_status"] = dev_status
     print(json.dumps(line), flush=True)
+    if dev_status:
+        raise SystemExit(f"decode calls reported device status {dev_status:#x}")
 
 
 def run_prefill(args, w):

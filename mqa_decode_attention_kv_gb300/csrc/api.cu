@@ -92,16 +92,18 @@ EncodeTiledFn encode_fn()
 }
 
 // 2-D map over int8 codes viewed as [num_blocks*page_size rows][head_dim cols],
-// boxes of 16 rows x head_dim, swizzled so that the kernels' fragment loads are
-// free of shared-memory bank conflicts.
-int make_code_map(CUtensorMap *m, const int8_t *codes, int num_blocks, int page_size, int head_dim)
+// boxes of box_rows rows x head_dim (16 by default; 64 for whole pages of 64),
+// swizzled so that the kernels' fragment loads are free of shared-memory bank
+// conflicts.
+int make_code_map(CUtensorMap *m, const int8_t *codes, int num_blocks, int page_size, int head_dim,
+                  int box_rows = kChunkTokens)
 {
     EncodeTiledFn f = encode_fn();
     if (f == nullptr)
         return MQA_ERR_CUDA;
     const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * (cuuint64_t)page_size};
     const cuuint64_t strides[1] = {(cuuint64_t)head_dim};
-    const cuuint32_t box[2] = {(cuuint32_t)head_dim, (cuuint32_t)kChunkTokens};
+    const cuuint32_t box[2] = {(cuuint32_t)head_dim, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle sw = head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(codes), dims, strides, box, estr,
@@ -147,6 +149,24 @@ int tiles_for(int L, int W)
 {
     const int lo = (W > 0 && L > W) ? L - W : 0;
     return (L - 1) / kTileTokens - lo / kTileTokens + 1;
+}
+
+// The balanced (persistent) tensor-core decode: CTAs it runs at most, and the
+// split count whose workspace holds its partials (2 slots of 32 heads per CTA).
+int tc_max_ctas(int head_dim, int heads)
+{
+    const int sms = sm_count();
+    return sms <= 0 ? 0 : sms * ctas_per_sm(head_dim, heads);
+}
+
+int tc_auto_splits(int batch, int heads, int head_dim)
+{
+    const long long g = tc_max_ctas(head_dim, heads);
+    const long long pairs = (long long)batch * ((heads + 31) / 32);
+    long long s = (2 * g + pairs - 1) / pairs;
+    if (s < 2)
+        s = 2;
+    return (int)(s > MQA_MAX_SPLITS ? MQA_MAX_SPLITS : s);
 }
 
 // Upper bound of tiles_for(L, W) over 1 <= L <= Lmax.
@@ -312,6 +332,11 @@ int mqa_decode_auto_splits(const mqa_batch *batch, int32_t window, int32_t num_q
         return rc;
     if (batch->batch == 0)
         return 1;
+    if (decode_uses_tc(head_dim, num_q_heads)) {
+        if (tc_max_ctas(head_dim, num_q_heads) <= 0)
+            return MQA_ERR_CUDA;
+        return tc_auto_splits(batch->batch, num_q_heads, head_dim);
+    }
     Plan p;
     rc = plan_decode(batch, window, num_q_heads, head_dim, 0, &p);
     return rc == MQA_OK ? p.num_splits : rc;
@@ -338,10 +363,23 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
     if (q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out))
         return MQA_ERR_INVALID_ARG;
     const int D = cache->head_dim;
+    const bool tc = decode_uses_tc(D, num_q_heads);
     Plan plan;
-    rc = plan_decode(batch, window, num_q_heads, D, num_splits, &plan);
-    if (rc != MQA_OK)
-        return rc;
+    if (tc) {
+        // tensor-core kernel: num_splits 1 = one CTA per (sequence, head group);
+        // otherwise balanced shares over the CTAs whose partials fit the split
+        // count's workspace (the automatic count fits every resident CTA)
+        plan.max_tiles = 0;
+        plan.tiles_per_split = 0;
+        plan.num_splits = num_splits == 1 ? 1 : (num_splits == 0 ? tc_auto_splits(batch->batch, num_q_heads, D)
+                                                                  : num_splits);
+        if (plan.num_splits > 1 && tc_max_ctas(D, num_q_heads) <= 0)
+            return MQA_ERR_CUDA;
+    } else {
+        rc = plan_decode(batch, window, num_q_heads, D, num_splits, &plan);
+        if (rc != MQA_OK)
+            return rc;
+    }
     DecodeArgs a;
     std::memset(&a, 0, sizeof a);
     if (plan.num_splits > 1) {
@@ -351,14 +389,37 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
         a.o_partial = static_cast<float *>(workspace);
         a.lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                           lse_offset(batch->batch, num_q_heads, D, plan.num_splits));
-        if (plan.num_splits <= kMaxFusedSplits)
+        if (tc || plan.num_splits <= kMaxFusedSplits)
             a.counters = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
                                                      counters_offset(batch->batch, num_q_heads, D, plan.num_splits));
+    }
+    if (tc) {
+        const long long pairs = (long long)batch->batch * head_groups(num_q_heads);
+        if (plan.num_splits > 1) {
+            long long g = tc_max_ctas(D, num_q_heads);
+            const long long fit = pairs * plan.num_splits / 2;  // CTAs whose 2 partial slots fit
+            a.persistent = 1;
+            a.persist_ctas = (int)(g < fit ? g : fit);
+        } else {
+            if (pairs > INT32_MAX)
+                return MQA_ERR_INVALID_ARG;
+            a.persistent = 0;
+            a.persist_ctas = (int)pairs;
+        }
     }
     if ((rc = make_code_map(&a.k_map, cache->k_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
         return rc;
     if ((rc = make_code_map(&a.v_map, cache->v_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
         return rc;
+    if (tc && cache->page_size == kTileTokens) {
+        // whole 64-token tiles (= pages) in one copy per tensor
+        if ((rc = make_code_map(&a.k_map64, cache->k_codes, cache->num_blocks, cache->page_size, D, kTileTokens)) !=
+            MQA_OK)
+            return rc;
+        if ((rc = make_code_map(&a.v_map64, cache->v_codes, cache->num_blocks, cache->page_size, D, kTileTokens)) !=
+            MQA_OK)
+            return rc;
+    }
     a.k_scale = cache->k_scale;
     a.v_scale = cache->v_scale;
     a.block_table = batch->block_table;
@@ -385,7 +446,7 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
         return MQA_ERR_CUDA;
     if (launch_decode(a, D, s) != cudaSuccess)
         return MQA_ERR_CUDA;
-    if (plan.num_splits > 1 && a.counters == nullptr &&
+    if (!tc && plan.num_splits > 1 && a.counters == nullptr &&
         launch_combine(a.o_partial, a.lse, a.batch, a.num_splits, num_q_heads, D, a.out, s) != cudaSuccess)
         return MQA_ERR_CUDA;
     return MQA_OK;

@@ -1,28 +1,41 @@
 // Decode attention on the 5th-generation tensor cores (tcgen05), head_dim 128,
-// 32 query heads per CTA.
+// groups of 32 query heads: one persistent, warp-specialised kernel.
 //
-// Per CTA (one split of one sequence, 8 warps, one CTA per SM):
-//  * keys arrive as 128-token blocks (two 64-token tiles = eight 16-token
-//    boxes) through a ring of RING blocks: per box one TMA tiled load of K
-//    codes, one of V codes (2-D maps over [num_blocks*page, 128] int8,
-//    128-byte swizzle) and two 64-byte bulk copies of the scales, each box on
-//    its own mbarrier; boxes outside [window start, L) are not fetched;
-//  * every int8 code is converted exactly once (exponent-bias trick, exact) into
-//    fp16 operand tiles in shared memory, K and V in one "core matrix" layout
-//    (8 token rows x 8 d, 16-byte rows) that serves as the K-major A operand of
-//    QK^T and as the MN-major A operand of PV;
-//  * MQA puts all 32 heads of a token into one row of a dense contraction:
-//      S^T[128 tokens x 32 heads]  = K[128 x 128] . Q^T      (tcgen05, TMEM)
-//      O^T[128 d x 32 heads]     += V^T[128 x 128] . P      (tcgen05, TMEM)
-//    one thread issues the MMAs; the accumulators live in tensor memory;
-//  * softmax: thread (token t, head half) reads its token's 16 scores with
-//    tcgen05.ld, applies the K scale, and exponentiates against a per-head
-//    reference maximum that only moves when a score exceeds it by more than
-//    2^8 (then the CTA rescales O in tensor memory and l in registers: rare);
-//    the V scale is folded into P' = p * s_v * 2^(6-E), 2^E a running
-//    power-of-two bound of the V scales, so fp16 P' never overflows;
-//  * output: bf16 directly, or fp32 partial O and lse per split (merged by the
-//    last split CTA for <= 16 splits, else by the combine kernel).
+// Work.  The call's (sequence b, head group g, 128-token key block) triples
+// form one list, ordered by b, then g, then block.  In the balanced mode CTA c
+// of the first G' = min(G, N) CTAs takes the contiguous share
+// [c*N/G', (c+1)*N/G') of the N list entries (never empty), so every CTA
+// streams the same number of blocks (+-1) whatever the length mix and
+// its pipeline runs across sequence boundaries without draining.  A piece of
+// a (b, g) pair that lies inside one share is the whole pair: its output is
+// written directly (bf16).  A pair cut by share boundaries leaves an fp32
+// partial (O, lse) per piece in slot 0 (the share's first piece) or 1 (its
+// last) of the CTA that computed it; the last piece to finish (an atomic
+// ticket per pair) merges them once its CTA has run out of blocks.  In the
+// whole-sequence mode CTA c computes pair c alone and needs no workspace.
+//
+// Roles (9 warps, one CTA per SM):
+//   warps 0-3  converters.  Thread t owns token row t of every block.  Waits
+//              for its TMA boxes, converts the K codes to fp16 straight into
+//              tensor memory (the A operand of S^T = K Q^T), the V codes to
+//              fp16 in shared memory (the A operand of O^T += V^T P'), copies
+//              the scales, and refills its warp's two boxes of the ring.  At
+//              a pair's first block it also converts Q (loaded into registers
+//              one block ahead) into the B operand of S^T = K Q^T.
+//   warps 4-7  softmax.  Thread t reads token t's 32 scores from tensor
+//              memory, applies the K scale, exponentiates against a per-head
+//              reference maximum that only moves when a score exceeds it by
+//              more than 2^8 (then O is rescaled in tensor memory: rare), and
+//              writes P' = p * s_v * 2^(6-E) (fp16; 2^E a running power-of-two
+//              bound of the V scales, so P' stays below 64).  At a piece's
+//              last block it normalises O and stores the output or partial.
+//   warp 8     lane 0 issues every tcgen05.mma and commit; the warp owns the
+//              tensor-memory allocation.
+//
+// Every int8 code is converted exactly once (exponent-bias trick, exact), the
+// scores and O accumulate in fp32 tensor memory, and every wait is bounded:
+// a wait that runs out raises a CTA-wide abort flag that makes all roles
+// leave, and the call reports MQA_DEV_TIMEOUT.
 #include <atomic>
 #include <cfloat>
 #include <math.h>
@@ -30,7 +43,6 @@
 #include "common.cuh"
 #include "kv_stage.cuh"
 #include "launch.h"
-#include "split_merge.cuh"
 #include "tc.cuh"
 
 namespace mqa {
@@ -38,56 +50,322 @@ namespace {
 
 struct TcCfg {
     static constexpr int D = 128;
-    static constexpr int NH = 32;                 // heads per CTA (MMA N)
-    static constexpr int BT = 128;                // tokens per block (MMA M of QK^T, K of PV)
-    static constexpr int BOXES = BT / kChunkTokens;  // 8
-    static constexpr int RING = 3;                // blocks in flight
-    static constexpr int THREADS = 256;
-    static constexpr int CODES = BT * D;          // int8 bytes of K (or V) of a block
-    static constexpr int STAGE = 2 * CODES + 1024;  // K codes, V codes, K and V scales (1 KB)
+    static constexpr int NH = 32;                    // heads per group (MMA N)
+    static constexpr int BT = 128;                   // tokens per block (M of S^T, K of O^T)
+    static constexpr int BOXES = BT / kChunkTokens;  // 8 TMA boxes of 16 tokens
+    static constexpr int RING = 5;                   // ring stages (codes in flight, then fp16 V)
+    static constexpr int THREADS = 320;              // 4 converter + 4 softmax warps, MMA warp, TMA warp
+    static constexpr int CODES = BT * D;             // int8 bytes of K (or V) of a block
+    static constexpr int STAGE = 2 * CODES;          // K codes, V codes; then fp16 V in place
     // shared memory (offsets from a 1024-aligned base)
     static constexpr int OFF_RING = 0;
-    static constexpr int OFF_KH = OFF_RING + RING * STAGE;    // fp16 K [128 tok][128 d], core layout
-    static constexpr int OFF_VH = OFF_KH + BT * D * 2;        // fp16 V, same layout
-    static constexpr int OFF_QH = OFF_VH + BT * D * 2;        // fp16 Q [32 h][128 d], core layout
-    static constexpr int OFF_PH = OFF_QH + NH * D * 2;        // fp16 P' [128 tok][32 h], core layout
-    static constexpr int OFF_RED = OFF_PH + BT * NH * 2;      // 256 fp32: reductions across warps
-    static constexpr int OFF_OK = OFF_RED + 256 * 4;          // [RING][8] box arrived
-    static constexpr int OFF_MISC = OFF_OK + RING * BOXES * 4;  // tmem base, flags
-    static constexpr int OFF_MBAR = OFF_MISC + 64;            // [RING][8] + S + O
-    static constexpr int SMEM_BYTES = OFF_MBAR + 8 * (RING * BOXES + 2) + 1024;
-    static constexpr uint32_t TMEM_COLS = 128;    // S (2 x 32) + O (32), power of two
-    // core-matrix strides (bytes): K/V tiles rows = tokens, Q rows = heads, P rows = tokens
-    static constexpr uint32_t KV_SR = 16 * 128;   // next 8 tokens
-    static constexpr uint32_t KV_SC = 128;        // next 8 d
-    static constexpr uint32_t Q_SR = 16 * 128;    // next 8 heads
-    static constexpr uint32_t Q_SC = 128;
-    static constexpr uint32_t P_SR = 4 * 128;     // next 8 tokens
-    static constexpr uint32_t P_SC = 128;         // next 8 heads
+    static constexpr int OFF_QH = OFF_RING + RING * STAGE;      // fp16 Q [32 h][128 d], core layout
+    static constexpr int OFF_QRAW = OFF_QH + NH * D * 2;        // bf16 Q [32 h][128 d] as copied (next piece)
+    static constexpr int OFF_PH = OFF_QRAW + NH * D * 2;        // [2] fp16 P' [128 tok][32 h], core layout
+    static constexpr int OFF_SC = OFF_PH + 2 * BT * NH * 2;     // [2][3][128] fp32: K scale, V scale, valid
+    static constexpr int OFF_RED = OFF_SC + 2 * 3 * BT * 4;     // softmax group: [4 warps][32] + [4] fp32
+    static constexpr int OFF_MREF = OFF_RED + 160 * 4;          // softmax group: reference maxima [32], factors [32]
+    static constexpr int OFF_CRED = OFF_MREF + 64 * 4;          // converter group: [4] fp32, gh[2]
+    static constexpr int OFF_OK = OFF_CRED + 16 * 4;            // [RING][8] box arrived
+    static constexpr int OFF_MISC = OFF_OK + RING * BOXES * 4;  // tmem base, abort flag, start, merges
+    static constexpr int OFF_MBAR = OFF_MISC + 256;
+    static constexpr int NBAR = 4 * RING + 14;  // tile full / free [RING][2] each, 6 x 2 hand-offs, Q full / free
+    static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
+    // tensor memory columns: S^T [2][32], O^T [2][32], fp16 K [2][64]
+    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t S_COL = 0, O_COL = 64, K_COL = 128;
+    // core-matrix strides (bytes): V rows = tokens, Q rows = heads, P rows = tokens.  The fp16
+    // V of converter warp w's tokens 32w .. 32w+31 overwrites the 8 KB of codes they came
+    // from: 8-token groups 0, 1 of the warp at K-half offset 4096w, groups 2, 3 at V-half
+    // offset 4096w, each group 16 core matrices (8 d each) of 128 B.
+    static constexpr uint32_t V_SR = 16 * 128;  // next 8 tokens (inside a 16-token MMA step)
+    static constexpr uint32_t V_SC = 128;       // next 8 d
+    static constexpr uint32_t Q_SR = 16 * 128;  // next 8 heads
+    static constexpr uint32_t Q_SC = 128;       // next 8 d
+    static constexpr uint32_t P_SR = 4 * 128;   // next 8 tokens
+    static constexpr uint32_t P_SC = 128;       // next 8 heads
+};
+static_assert(TcCfg::SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+// Mbarrier wait with a suspend hint: a waiting warp sleeps until the phase
+// completes instead of polling (eight warps polling would crowd the shared-
+// memory pipe that the converters, the TMA and the tensor core use).
+__device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) { return mbar_try_wait(bar, parity); }
+
+// Bounded wait that also gives up once another role has raised the abort
+// flag; a wait that runs out raises it.  Returns false when giving up.
+__device__ __noinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag);
+
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    return mbar_poll(bar, parity) || wait_phase_slow(bar, parity, abort_flag);
+}
+
+// The polling loop, out of line: the many wait sites stay small.
+__device__ __noinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 16; ++i)
+            if (mbar_poll(bar, parity))
+                return true;
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void named_bar(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Barrier over n threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// Parity of the phase of a two-buffer hand-off barrier that carries item i.
+__device__ __forceinline__ uint32_t ph2(int i) { return (uint32_t)(i >> 1) & 1u; }
+
+// Reduce 32 per-head values over the 32 lanes of a warp with 31 shuffles (a
+// butterfly that halves the values each lane keeps at every step): lane L
+// returns the reduction of head L.  v is consumed.
+template <bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int k = 0; k < s; ++k) {
+            const float send = up ? v[k] : v[k + s];
+            const float keep = up ? v[k + s] : v[k];
+            const float got = __shfl_xor_sync(0xffffffffu, send, s);
+            v[k] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
+}
+
+// A: tensor memory, B: shared memory descriptor.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred pa;\n\tsetp.ne.u32 pa, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Key blocks of a sequence of length L: the 64-token tiles from the one
+// holding the window start to the one holding L-1, paired into 128-token
+// blocks (the last block may hold a single tile).  0 for an invalid length.
+__device__ __forceinline__ int seq_blocks(int L, int window, int max_seq_len, int &t_first, int &lo)
+{
+    t_first = 0;
+    lo = 0;
+    if (L < 1 || L > max_seq_len)
+        return 0;
+    lo = (window > 0 && L > window) ? L - window : 0;
+    t_first = lo / kTileTokens;
+    const int t_last = (L - 1) / kTileTokens;
+    return (t_last - t_first + 2) >> 1;
+}
+
+// Position in the (sequence, head group, block) list.
+struct Cursor {
+    int b, g, blk;      // sequence, head group, block of the sequence
+    int nblk;           // blocks of sequence b
+    int t_first, lo, L; // first tile, window start, length of sequence b
 };
 
-// One box of a ring block: K and V codes (16 rows x 128 B each, TMA with
-// 128-byte swizzle) and their 16 + 16 scales.
-__device__ __forceinline__ void issue_block_box(const DecodeArgs &a, int32_t id, uint8_t *stage, uint64_t *bar,
-                                                uint32_t *box_ok, int T, int c, int box)
+// Load sequence b's shape into the cursor; then skip sequences without blocks.
+__device__ __forceinline__ void cursor_seek(Cursor &c, const DecodeArgs &a)
 {
-    constexpr int D = TcCfg::D;
-    const int t0 = T * kTileTokens + c * kChunkTokens;
+    while (c.b < a.batch) {
+        c.L = __ldg(a.seq_lens + c.b);
+        c.nblk = seq_blocks(c.L, a.window, a.max_seq_len, c.t_first, c.lo);
+        if (c.nblk > 0)
+            return;
+        ++c.b;
+        c.g = 0;
+        c.blk = 0;
+    }
+}
+
+__device__ __forceinline__ void cursor_next(Cursor &c, const DecodeArgs &a, int groups)
+{
+    if (++c.blk < c.nblk)
+        return;
+    c.blk = 0;
+    if (++c.g < groups)
+        return;
+    c.g = 0;
+    ++c.b;
+    cursor_seek(c, a);
+}
+
+// The CTA whose share holds list entry x (the largest c with floor(c*N/G) <= x).
+__device__ __forceinline__ int cta_of(long long x, long long N, int G)
+{
+    return (int)(((x + 1) * G - 1) / N);
+}
+
+// Cache row of the first token of box c of tile T in block `id`, or -1 when
+// the box is not fetched (kNoBlock, or an id outside the pool: reported).
+__device__ __forceinline__ int box_row(const DecodeArgs &a, int32_t id, int T, int c)
+{
     const bool ok = id >= 0 && id < a.num_blocks;
     if (!ok && id != kNoBlock)
         set_status(a.dev_status, MQA_DEV_BAD_BLOCK);
-    *box_ok = ok ? 1u : 0u;
-    if (!ok) {
-        mbar_arrive_expect_tx(bar, 0);
-        return;
+    return ok ? id * a.page_size + (T * kTileTokens + c * kChunkTokens) % a.page_size : -1;
+}
+
+// Block id of box c (16 tokens) of tile t (64 tokens, 0 or 1) of the block at
+// cursor position p; kNoBlock when the box lies outside [lo, L).
+__device__ __forceinline__ int32_t fetch_tile_box_id(const DecodeArgs &a, const Cursor &p, int t, int c)
+{
+    const int T = p.t_first + 2 * p.blk + t;
+    return T <= (p.L - 1) / kTileTokens
+               ? fetch_box_block(a.block_table + (size_t)p.b * a.max_blocks, a.page_size, T, c, p.lo, p.L)
+               : kNoBlock;
+}
+
+// Both tiles of the block at p into ring stage `stage`, issued by the TMA warp
+// (every lane calls; lane 4t + c holds the id of box c of tile t).  A tile
+// inside [lo, L) on one 64-token page goes as one 64-row copy per tensor, any
+// other tile as its 16-row boxes that overlap [lo, L).  One arrival per tile
+// on bars[t] with its byte count; box_ok[4t + c] records whether box c comes.
+__device__ __forceinline__ void issue_block(const DecodeArgs &a, const Cursor &p, int lane, int32_t idc,
+                                            uint8_t *stage, uint64_t *bars, uint32_t *oks)
+{
+    constexpr int D = TcCfg::D;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int T = p.t_first + 2 * p.blk + t;
+        const int c = lane - 4 * t;
+        const bool mine = c >= 0 && c < 4;
+        const int row = mine ? box_row(a, idc, T, c) : -1;
+        const uint32_t okmask = (__ballot_sync(0xffffffffu, row >= 0) >> (4 * t)) & 0xfu;
+        const int row0 = __shfl_sync(0xffffffffu, row, 4 * t);
+        const bool whole = a.page_size == kTileTokens && okmask == 0xfu && T * kTileTokens >= p.lo &&
+                           T * kTileTokens + kTileTokens <= p.L;
+        if (mine)
+            oks[4 * t + c] = row >= 0 ? 1u : 0u;
+        __syncwarp();  // the flags are written before the arrival (a tile with nothing to fetch completes on it)
+        if (lane == 0)
+            mbar_arrive_expect_tx(bars + t, 2u * (uint32_t)__popc(okmask) * kChunkTokens * D);
+        __syncwarp();
+        if (whole) {
+            if (lane == 0) {
+                tma_load_2d(stage + t * kTileTokens * D, &a.k_map64, 0, row0, bars + t);
+                tma_load_2d(stage + TcCfg::CODES + t * kTileTokens * D, &a.v_map64, 0, row0, bars + t);
+            }
+        } else if (row >= 0) {
+            const int box = 4 * t + c;
+            tma_load_2d(stage + box * kChunkTokens * D, &a.k_map, 0, row, bars + t);
+            tma_load_2d(stage + TcCfg::CODES + box * kChunkTokens * D, &a.v_map, 0, row, bars + t);
+        }
     }
-    const int row = id * a.page_size + (t0 % a.page_size);
-    float *ks = reinterpret_cast<float *>(stage + 2 * TcCfg::CODES);
-    mbar_arrive_expect_tx(bar, 2 * kChunkTokens * D + 2 * kChunkTokens * 4);
-    tma_load_2d(stage + box * kChunkTokens * D, &a.k_map, 0, row, bar);
-    tma_load_2d(stage + TcCfg::CODES + box * kChunkTokens * D, &a.v_map, 0, row, bar);
-    bulk_load(ks + box * kChunkTokens, a.k_scale + row, kChunkTokens * 4, bar);
-    bulk_load(ks + TcCfg::BT + box * kChunkTokens, a.v_scale + row, kChunkTokens * 4, bar);
+}
+
+// This thread's token scales for the block at p (token tok: box tok >> 4), 0
+// when its box is not fetched.
+__device__ __forceinline__ void load_token_scales(const DecodeArgs &a, const Cursor &p, int tok, int32_t id,
+                                                  float &ks, float &vs)
+{
+    const int row = box_row(a, id, p.t_first + 2 * p.blk + (tok >> 6), (tok >> 4) & 3);
+    ks = row >= 0 ? __ldg(a.k_scale + row + (tok & 15)) : 0.f;
+    vs = row >= 0 ? __ldg(a.v_scale + row + (tok & 15)) : 0.f;
+}
+
+// Shared-memory descriptor plus a byte offset (the address field counts 16 B).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
+// Q row of head `lane` of the group at p (128 bf16 = 16 uint4) into registers;
+// the four uint4 of the d range warp w converts (32w .. 32w+31) come first.
+__device__ __forceinline__ void load_q_row(const DecodeArgs &a, const Cursor &p, int w, int lane, uint4 (&qv)[16])
+{
+    const int h = p.g * TcCfg::NH + lane;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)p.b * a.num_q_heads + h) * TcCfg::D);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        qv[k] = h < a.num_q_heads ? __ldg(src + ((k + 4 * w) & 15)) : make_uint4(0, 0, 0, 0);
+}
+
+// O^T += V^T(j) P'(j) for block j into the O buffer of its piece (MMA thread).
+// Returns false when a wait gave up.
+__device__ __forceinline__ bool issue_pv(int j, uint32_t first_bits, int &piece, int &n_pv, uint32_t tmem,
+                                         uint64_t vdesc0, uint64_t pdesc0, uint64_t *pready, uint64_t *vready,
+                                         uint64_t *ofree, uint64_t *odone, uint64_t *sfree, volatile int *abort_flag)
+{
+    using C = TcCfg;
+    constexpr uint32_t IDESC_PV = umma_idesc_f16(128, C::NH, true, true);
+    const int jb = j & 1;
+    if (!wait_phase(pready + jb, ph2(j), abort_flag) || !wait_phase(vready + jb, ph2(j), abort_flag))
+        return false;
+    const bool first = (first_bits >> (j & 31)) & 1u;
+    if (first) {
+        ++piece;
+        // the O buffer of piece - 2 must have been read by its epilogue
+        if (piece >= 2 && !wait_phase(ofree + (piece & 1), ph2(piece - 2), abort_flag))
+            return false;
+    }
+    tc_fence_after();
+    const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * C::NH;
+    // V: fp16 in place in ring stage j % RING; 16-token step kk = token groups 2kk, 2kk+1 of
+    // converter warp kk / 2, in the K half (kk even) or the V half (kk odd)
+    const uint64_t vd = desc_add(vdesc0, (j % C::RING) * C::STAGE), pd = desc_add(pdesc0, jb * C::BT * C::NH * 2);
+#pragma unroll
+    for (int kk = 0; kk < C::BT / 16; ++kk)
+        umma_f16(tmem + o_col, desc_add(vd, (kk & 1) * C::CODES + (kk >> 1) * 4096), desc_add(pd, kk * 2 * C::P_SR),
+                 IDESC_PV, !first || kk > 0);
+    umma_commit(odone + jb);
+    umma_commit(sfree + (j % C::RING));  // the stage's V is read: the TMA warp may refill it
+    ++n_pv;
+    return true;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Partial-output row of piece s (0 = the pair's first piece, in CTA c_lo) of a
+// merged pair: CTA c_lo + s, slot slot_lo for s == 0 else 0, head jh.
+__device__ __forceinline__ size_t merge_row(int c_lo, int s, int slot_lo, int jh)
+{
+    return (size_t)(2 * (c_lo + s) + (s == 0 ? slot_lo : 0)) * TcCfg::NH + jh;
 }
 
 }  // namespace
@@ -95,389 +373,818 @@ __device__ __forceinline__ void issue_block_box(const DecodeArgs &a, int32_t id,
 __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __grid_constant__ DecodeArgs a)
 {
     using C = TcCfg;
-    constexpr int D = C::D, NH = C::NH, RING = C::RING;
+    constexpr int D = C::D, NH = C::NH, RING = C::RING, BT = C::BT;
+    constexpr int BAR_SM = 1;  // named barrier of the softmax warps
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *kh = base + C::OFF_KH;
-    uint8_t *vh = base + C::OFF_VH;
     uint8_t *qh = base + C::OFF_QH;
+    uint8_t *qraw = base + C::OFF_QRAW;
     uint8_t *ph = base + C::OFF_PH;
+    float *sc = reinterpret_cast<float *>(base + C::OFF_SC);
     float *red = reinterpret_cast<float *>(base + C::OFF_RED);
+    float *mref = reinterpret_cast<float *>(base + C::OFF_MREF);  // [32] per-head reference (log2 domain)
+    float *ofac_s = mref + NH;                                     // [32] per-head O rescale factors
+    float *cred = reinterpret_cast<float *>(base + C::OFF_CRED);
     uint32_t *box_ok = reinterpret_cast<uint32_t *>(base + C::OFF_OK);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
-    volatile int *flag = reinterpret_cast<int *>(base + C::OFF_MISC + 8);
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][8] boxes
-    uint64_t *mbar_s = mbar + RING * C::BOXES;
-    uint64_t *mbar_o = mbar_s + 1;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 4);
+    int *start_pos = reinterpret_cast<int *>(base + C::OFF_MISC + 16);          // b, g, blk, n
+    long long *share = reinterpret_cast<long long *>(base + C::OFF_MISC + 32);  // first entry, N, CTAs
+    int *merges = reinterpret_cast<int *>(base + C::OFF_MISC + 64);             // count, [2][5]
+    static_assert(32 + 3 * 8 <= 64 && 64 + 11 * 4 <= 256, "misc layout");
+    uint64_t *tfull = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][2] tile codes landed (TMA)
+    uint64_t *tfree = tfull + 2 * RING;         // [RING] stage free: O^T of its block done (tensor core)
+    uint64_t *kready = tfree + 2 * RING;        // [2] K in tensor memory, scales, Q   (4 converter warps)
+    uint64_t *vready = kready + 2;              // [2] fp16 V in shared memory          (4 converter warps)
+    uint64_t *pready = vready + 2;              // [2] P' written, S read               (4 softmax warps)
+    uint64_t *sfull = pready + 2;               // [2] S^T = K Q^T done                 (tensor core)
+    uint64_t *odone = sfull + 2;                // [2] O^T += V^T P' done               (tensor core)
+    uint64_t *ofree = odone + 2;                // [2] a piece's O read by its epilogue (4 softmax warps)
+    uint64_t *qfull = ofree + 2;                // raw Q of the next piece landed      (bulk copy)
+    uint64_t *qfree = qfull + 1;                // raw Q read by every converter warp  (4 converter warps)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tok = 32 * (warp & 3) + lane;  // token row of a block = tensor-memory lane
-    const int hh = warp >> 2;                // head half: heads 16hh .. 16hh+15 of the CTA
-    const int split = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * NH;
-    const bool split_mode = a.num_splits > 1;
+    const int groups = (a.num_q_heads + NH - 1) / NH;
+    const int G = gridDim.x;
+    const int cta = blockIdx.x;
+    const bool balanced = a.persistent != 0;
 
-    // ---- key range of this CTA (in 64-token tiles)
-    const int L = __ldg(a.seq_lens + b);
-    const int lo = (L >= 1 && a.window > 0 && L > a.window) ? L - a.window : 0;
-    const int t_first = lo / kTileTokens;
-    const int t_last = (L - 1) / kTileTokens;
-    const bool bad = L < 1 || L > a.max_seq_len ||
-                     (t_last - t_first + 1) > a.tiles_per_split * a.num_splits;
-    const int tb = t_first + split * a.tiles_per_split;
-    const int te = min(tb + a.tiles_per_split, t_last + 1);
-    if (bad || tb >= te) {
-        if (bad && tid == 0 && split == 0)
-            set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);
-        for (int r = tid; r < NH; r += blockDim.x) {
-            const int h = h0 + r;
-            if (h >= a.num_q_heads)
-                continue;
-            if (split_mode)
-                a.lse[((size_t)b * a.num_splits + split) * a.num_q_heads + h] = -INFINITY;
-            if (!split_mode || (bad && split == 0)) {
-                uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)b * a.num_q_heads + h) * D);
-                for (int j = 0; j < D / 8; ++j)
-                    dst[j] = make_uint4(0, 0, 0, 0);
+    // ---- this CTA's share of the (sequence, group, block) list
+    if (balanced && a.batch <= C::THREADS) {
+        // one pass (a sequence per thread): its blocks, the block-wide prefix and total
+        int *wsum = reinterpret_cast<int *>(red);
+        int nb = 0;
+        if (tid < a.batch) {
+            int tf, lo;
+            nb = seq_blocks(__ldg(a.seq_lens + tid), a.window, a.max_seq_len, tf, lo);
+            if (nb == 0 && tid % G == cta) {
+                set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.out + (size_t)tid * a.num_q_heads * D);
+                for (int k = 0; k < a.num_q_heads * D / 8; ++k)
+                    dst[k] = make_uint4(0, 0, 0, 0);
             }
         }
-        return;
+        int x = nb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off)
+                x += y;
+        }
+        if (lane == 31)
+            wsum[warp] = x;
+        __syncthreads();
+        long long pre = 0, total = 0;
+        for (int w = 0; w < C::THREADS / 32; ++w) {
+            if (w < warp)
+                pre += wsum[w];
+            total += wsum[w];
+        }
+        const long long NB = total * groups;
+        const int Ge = (int)(NB < G ? NB : G);
+        const long long first = cta < Ge ? NB * cta / Ge : 0, last = cta < Ge ? NB * (cta + 1) / Ge : 0;
+        const long long incl = (pre + x) * groups, excl = (pre + x - nb) * groups;
+        if (tid == 0) {
+            share[0] = first;
+            share[1] = NB;
+            share[2] = Ge;
+            start_pos[3] = (int)(last - first);
+        }
+        if (nb > 0 && last > first && excl <= first && first < incl) {
+            const int r = (int)(first - excl);
+            start_pos[0] = tid;
+            start_pos[1] = r / nb;
+            start_pos[2] = r % nb;
+        }
+        __syncthreads();
+    } else if (balanced) {
+        int *wsum = reinterpret_cast<int *>(red);
+        // pass 1: blocks per group over all sequences; sequences without blocks
+        // (invalid length) get a zero output from CTA b % G and a status bit
+        long long mine = 0;
+        for (int bb = tid; bb < a.batch; bb += C::THREADS) {
+            int tf, lo;
+            const int L = __ldg(a.seq_lens + bb);
+            const int nb = seq_blocks(L, a.window, a.max_seq_len, tf, lo);
+            mine += nb;
+            if (nb == 0 && bb % G == cta) {
+                set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.out + (size_t)bb * a.num_q_heads * D);
+                for (int k = 0; k < a.num_q_heads * D / 8; ++k)
+                    dst[k] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            mine += __shfl_xor_sync(0xffffffffu, mine, off);
+        if (lane == 0)
+            reinterpret_cast<long long *>(wsum)[warp] = mine;
+        __syncthreads();
+        long long NB = 0;
+        for (int w = 0; w < C::THREADS / 32; ++w)
+            NB += reinterpret_cast<long long *>(wsum)[w];
+        NB *= groups;
+        // shares over Ge = min(G, N) CTAs, so that every share is non-empty and the
+        // pieces of a cut pair lie in consecutive CTAs; CTAs from Ge on have none
+        const int Ge = (int)(NB < G ? NB : G);
+        const long long first = cta < Ge ? NB * cta / Ge : 0, last = cta < Ge ? NB * (cta + 1) / Ge : 0;
+        if (tid == 0) {
+            share[0] = first;
+            share[1] = NB;
+            share[2] = Ge;
+            start_pos[3] = (int)(last - first);
+        }
+        __syncthreads();
+        // pass 2: the sequence holding entry `first` (its prefix of blocks x groups
+        // is <= first < prefix + its blocks x groups)
+        long long run = 0;
+        for (int b0 = 0; b0 < a.batch && last > first; b0 += C::THREADS) {
+            const int bb = b0 + tid;
+            int tf, lo, nb = 0;
+            if (bb < a.batch)
+                nb = seq_blocks(__ldg(a.seq_lens + bb), a.window, a.max_seq_len, tf, lo);
+            int x = nb;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off)
+                    x += y;
+            }
+            __syncthreads();  // wsum reuse
+            if (lane == 31)
+                wsum[warp] = x;
+            __syncthreads();
+            long long pre = run;
+            int chunk = 0;
+            for (int w = 0; w < C::THREADS / 32; ++w) {
+                if (w < warp)
+                    pre += wsum[w];
+                chunk += wsum[w];
+            }
+            const long long incl = (pre + x) * groups, excl = (pre + x - nb) * groups;
+            if (nb > 0 && excl <= first && first < incl) {
+                const int r = (int)(first - excl);
+                start_pos[0] = bb;
+                start_pos[1] = r / nb;
+                start_pos[2] = r % nb;
+            }
+            run += chunk;
+        }
+        __syncthreads();
+    } else {
+        // whole-sequence mode: CTA c computes (sequence c / groups, group c % groups)
+        if (tid == 0) {
+            const int bb = cta / groups, gg = cta % groups;
+            int tf, lo;
+            const int nb = seq_blocks(__ldg(a.seq_lens + bb), a.window, a.max_seq_len, tf, lo);
+            start_pos[0] = bb;
+            start_pos[1] = gg;
+            start_pos[2] = 0;
+            start_pos[3] = nb;
+            share[0] = 0;
+            share[1] = 0;
+            share[2] = G;
+            if (nb == 0)
+                set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);
+        }
+        __syncthreads();
+        if (start_pos[3] == 0) {
+            const int bb = cta / groups, gg = cta % groups;
+            for (int r = tid; r < NH * D / 8; r += C::THREADS) {
+                const int h = gg * NH + r / (D / 8);
+                if (h < a.num_q_heads)
+                    reinterpret_cast<uint4 *>(a.out + ((size_t)bb * a.num_q_heads + h) * D)[r % (D / 8)] =
+                        make_uint4(0, 0, 0, 0);
+            }
+        }
     }
-    const int n_tiles = te - tb;
-    const int n_blocks = (n_tiles + 1) / 2;
-    const int32_t *table = a.block_table + (size_t)b * a.max_blocks;
+    const int n = start_pos[3];
+    if (n <= 0)
+        return;  // uniform: nothing to compute
+    const long long list_first = share[0], list_n = share[1];
+    const int Ge = (int)share[2];  // CTAs with a share (balanced mode)
+    Cursor c0;
+    c0.b = start_pos[0];
+    c0.g = start_pos[1];
+    c0.blk = start_pos[2];
+    cursor_seek(c0, a);  // loads the shape of sequence c0.b (which has blocks)
 
     // ---- set-up: barriers, tensor memory, the first RING blocks in flight
     if (tid == 0) {
-        for (int s = 0; s < RING * C::BOXES + 2; ++s)
-            mbar_init(mbar + s, 1);
-        *flag = 0;
+        for (int s = 0; s < 2 * RING; ++s) {
+            mbar_init(tfull + s, 1);
+            mbar_init(tfree + s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(kready + s, 4);
+            mbar_init(vready + s, 4);
+            mbar_init(pready + s, 4);
+            mbar_init(sfull + s, 1);
+            mbar_init(odone + s, 1);
+            mbar_init(ofree + s, 4);
+        }
+        mbar_init(qfull, 1);
+        mbar_init(qfree, 4);
+        *abort_flag = 0;
+        merges[0] = 0;
         fence_mbar_init();
     }
-    if (warp == 0)
+    if (warp == 8)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // warp w produces box w of every block: tile (w / 4) of the block, box (w % 4) of the tile
-    const int my_tile = warp >> 2, my_c = warp & 3;
-    if (lane == 0)
-        for (int j = 0; j < n_blocks && j < RING; ++j) {
-            const int T = tb + 2 * j + my_tile;
-            const int32_t id = T < te ? fetch_box_block(table, a.page_size, T, my_c, lo, L) : kNoBlock;
-            issue_block_box(a, id, base + C::OFF_RING + j * C::STAGE, mbar + j * C::BOXES + warp,
-                            box_ok + j * C::BOXES + warp, T, my_c, warp);
-        }
-
-    // ---- Q: 32 heads x 128 d, scaled by one power of two 2^e (exact in fp16), into
-    // the core-matrix layout of the QK^T B operand (rows = heads, K-major)
-    {
-        // thread covers head (tid >> 3), d = 16*(tid & 7) .. +15
-        const int qr = tid >> 3, qc = (tid & 7) * 16;
-        const int h = h0 + qr;
-        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-        if (h < a.num_q_heads) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)b * a.num_q_heads + h) * D + qc);
-            v0 = __ldg(src);
-            v1 = __ldg(src + 1);
-        }
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        float m = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0)
-            red[warp] = m;
-        __syncthreads();
-        m = red[0];
-#pragma unroll
-        for (int k = 1; k < 8; ++k)
-            m = fmaxf(m, red[k]);
-        int e = 0;
-        if (m > 0.f && isfinite(m)) {
-            int x;
-            frexpf(m, &x);
-            e = 14 - x;
-            e = e < -120 ? -120 : (e > 120 ? 120 : e);
-        }
-        const float f = exp2i(e);
-        uint32_t hv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            hv[k] = pack_half2(__uint_as_float(w[k] << 16) * f, __uint_as_float(w[k] & 0xffff0000u) * f);
-        *reinterpret_cast<uint4 *>(qh + core_off(qr, qc, C::Q_SR, C::Q_SC)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<uint4 *>(qh + core_off(qr, qc + 8, C::Q_SR, C::Q_SC)) =
-            make_uint4(hv[4], hv[5], hv[6], hv[7]);
-        if (tid == 0)
-            red[8] = a.q_scale_log2 * exp2i(-e);  // log2-domain factor of the raw scores
-    }
-    fence_proxy_async();
-    __syncthreads();
-    const float gh = red[8];
-
-    float m_ref[16], l_acc[16];  // heads 16hh + j: reference max (raw-score units), this thread's sum of p
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        m_ref[j] = -INFINITY;
-        l_acc[j] = 0.f;
-    }
-    int E_run = -100;       // running power-of-two bound of the V scales
-    bool o_valid = false;   // O has been written by a first PV
-    const uint32_t tl = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's tensor-memory lanes
-    constexpr uint32_t O_COL = 64;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's tensor-memory lanes
     constexpr uint32_t IDESC_QK = umma_idesc_f16(128, NH, false, false);
-    constexpr uint32_t IDESC_PV = umma_idesc_f16(128, NH, true, true);
-    const uint32_t kh_u = smem_u32(kh), vh_u = smem_u32(vh), qh_u = smem_u32(qh), ph_u = smem_u32(ph);
-    int blk = 0;
-    int n_issued = min(n_blocks, RING);  // blocks whose boxes are in flight or landed
-    int n_qk = 0, n_pv = 0;              // MMA groups issued (same in every thread)
-    for (; blk < n_blocks; ++blk) {
-        const int r = blk % RING;
-        uint8_t *st = base + C::OFF_RING + r * C::STAGE;
-        const float *ks = reinterpret_cast<const float *>(st + 2 * C::CODES);
-        const float *vs = ks + C::BT;
-        const int mybox = tok >> 4;
-        // block id of my box of block blk + RING, fetched ahead of its issue
-        int32_t id_next = kNoBlock;
-        const int T_next = tb + 2 * (blk + RING) + my_tile;
-        if (lane == 0 && blk + RING < n_blocks && T_next < te)
-            id_next = fetch_box_block(table, a.page_size, T_next, my_c, lo, L);
-        if (!mbar_wait_bounded(mbar + r * C::BOXES + mybox, (uint32_t)(blk / RING) & 1u))
-            *flag = 1;
-        const bool ok = box_ok[r * C::BOXES + mybox] != 0;
-        const int pos = (tb + 2 * blk) * kTileTokens + tok;
-        const bool valid = ok && pos >= lo && pos < L;
-        // the previous PV reads V, P and writes O: wait before touching them
-        if (blk > 0) {
-            if (!mbar_wait_bounded(mbar_o, (uint32_t)(blk - 1) & 1u))
-                *flag = 1;
-            tc_fence_after();
-        }
-        // ---- convert this token's K and V codes, d in [64hh, 64hh+64), to fp16 (exact)
+
+    if (warp < 4) {
+        // ================================================================ converters
+        const int tok = tid;  // token row of every block = tensor-memory lane
+        const int my_tile = warp >> 1;            // warps 0, 1 read tile 0 of a block; warps 2, 3 tile 1
+        Cursor cur = c0, pre = c0;
+        int n_issued = 0, q_issued = 0;
+        float ksr[RING], vsr[RING];  // scales of this thread's token in blocks i .. i+RING-1
         {
-            const uint8_t *krow = st + tok * D;
-            const uint8_t *vrow = st + C::CODES + tok * D;
+            // scales of this thread's token in the first RING blocks: ids first, then the loads
+            int32_t ids[RING];
+            Cursor p = c0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = 4 * hh + q;  // 16-byte chunk of the row (d = 16j .. 16j+15)
-                const uint32_t so = (uint32_t)(j ^ (tok & 7)) << 4;
-                const uint4 kv = *reinterpret_cast<const uint4 *>(krow + so);
-                const uint4 vv = *reinterpret_cast<const uint4 *>(vrow + so);
-                uint32_t k8[8], v8[8];
-                i8x4_to_f16x2x2(kv.x, k8[0], k8[1]);
-                i8x4_to_f16x2x2(kv.y, k8[2], k8[3]);
-                i8x4_to_f16x2x2(kv.z, k8[4], k8[5]);
-                i8x4_to_f16x2x2(kv.w, k8[6], k8[7]);
-                i8x4_to_f16x2x2(vv.x, v8[0], v8[1]);
-                i8x4_to_f16x2x2(vv.y, v8[2], v8[3]);
-                i8x4_to_f16x2x2(vv.z, v8[4], v8[5]);
-                i8x4_to_f16x2x2(vv.w, v8[6], v8[7]);
-                const uint32_t o0 = core_off(tok, 16 * j, C::KV_SR, C::KV_SC);
-                const uint32_t o1 = core_off(tok, 16 * j + 8, C::KV_SR, C::KV_SC);
-                *reinterpret_cast<uint4 *>(kh + o0) = make_uint4(k8[0], k8[1], k8[2], k8[3]);
-                *reinterpret_cast<uint4 *>(kh + o1) = make_uint4(k8[4], k8[5], k8[6], k8[7]);
-                *reinterpret_cast<uint4 *>(vh + o0) = make_uint4(v8[0], v8[1], v8[2], v8[3]);
-                *reinterpret_cast<uint4 *>(vh + o1) = make_uint4(v8[4], v8[5], v8[6], v8[7]);
+            for (int j = 0; j < RING; ++j) {
+                ids[j] = j < n ? fetch_tile_box_id(a, p, tok >> 6, (tok >> 4) & 3) : kNoBlock;
+                cursor_next(p, a, groups);
             }
-        }
-        const float ksv = ks[tok], vsv = vs[tok];
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();  // B1: fp16 K/V ready; ring slot r fully read
-        if (*flag)
-            break;
-        tc_fence_after();
-        if (blk + RING < n_blocks) {
-            if (lane == 0)
-                issue_block_box(a, T_next < te ? id_next : kNoBlock, st, mbar + r * C::BOXES + warp,
-                                box_ok + r * C::BOXES + warp, T_next, my_c, warp);
-            ++n_issued;
-        }
-        // ---- S^T = K Q^T on the tensor cores
-        const uint32_t s_col = (uint32_t)(blk & 1) * NH;
-        if (tid == 0) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                umma_f16(tmem + s_col, umma_sdesc(kh_u + kk * 2 * C::KV_SC, C::KV_SC, C::KV_SR),
-                         umma_sdesc(qh_u + kk * 2 * C::Q_SC, C::Q_SC, C::Q_SR), IDESC_QK, kk > 0);
-            umma_commit(mbar_s);
+            for (int j = 0; j < RING; ++j) {
+                ksr[j] = vsr[j] = 0.f;
+                if (j < n) {
+                    load_token_scales(a, pre, tok, ids[j], ksr[j], vsr[j]);
+                    cursor_next(pre, a, groups);
+                    ++n_issued;
+                }
+            }
+            // the first piece's Q (bf16, 32 heads x 256 B, contiguous)
+            if (warp == 0 && lane == 0) {
+                mbar_arrive_expect_tx(qfull, NH * D * 2);
+                bulk_load(qraw, a.q + ((size_t)c0.b * a.num_q_heads + c0.g * NH) * D, NH * D * 2, qfull);
+            }
+            q_issued = 1;
         }
-        ++n_qk;
-        if (!mbar_wait_bounded(mbar_s, (uint32_t)blk & 1u))
-            *flag = 1;
-        tc_fence_after();
-        uint32_t sr[16];
-        tmem_ld16(tmem + tl + s_col + 16 * hh, sr);
-        tmem_wait_ld();
-        // ---- softmax against the reference maxima
-        float y[16], dd[16];
-        bool need = valid && !(vsv <= exp2i(E_run));
+        int32_t idn = kNoBlock;  // this token's box id in block n_issued, fetched an iteration ahead
+        int piece = -1;
+        int i = 0;
+        for (; i < n; ++i) {
+            const int r = i % RING, buf = i & 1;
+            uint8_t *st = base + C::OFF_RING + r * C::STAGE;
+            const bool first = (i == 0) || cur.blk == 0;
+            if (n_issued < n)  // used by this iteration's scale loads
+                idn = fetch_tile_box_id(a, pre, tok >> 6, (tok >> 4) & 3);
+            bool ok = wait_phase(tfull + 2 * r + my_tile, (uint32_t)(i / RING) & 1u, abort_flag);
+            if (i >= 2) {
+                // K buffer [buf] free once S^T(i-2) is done; scale slot [buf] once softmax(i-2) is
+                ok = ok && wait_phase(sfull + buf, ph2(i - 2), abort_flag);
+                ok = ok && wait_phase(pready + buf, ph2(i - 2), abort_flag);
+            }
+            if (first) {
+                ok = ok && wait_phase(qfull, (uint32_t)(piece + 1) & 1u, abort_flag);  // this piece's raw Q
+                if (i >= 1)  // fp16 Q is single-buffered: every S^T(i-1) must be done
+                    ok = ok && wait_phase(sfull + ((i - 1) & 1), ph2(i - 1), abort_flag);
+            }
+            if (!__all_sync(0xffffffffu, ok))
+                break;
+            tc_fence_after();
+            if (first) {
+                // ---- Q of this piece, scaled by one power of two 2^e (exact in fp16): lane =
+                // head; pass 1 takes the max over the 32 x 128 values (chunks read in a
+                // lane-rotated order: no bank conflicts), pass 2 converts this warp's d range
+                ++piece;
+                const uint8_t *qrow = qraw + lane * D * 2;
+                float m = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            y[j] = valid ? __uint_as_float(sr[j]) * ksv : -INFINITY;
-            dd[j] = valid ? fmaf(y[j], gh, -m_ref[j] * gh) : -INFINITY;
-            need |= valid && !(dd[j] <= 8.f);
-        }
-        if (__syncthreads_or(need)) {  // B2 (rare after the first block): move the references
+                for (int k = 0; k < 16; ++k) {
+                    const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * ((k + lane) & 15));
+                    const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float m = y[j];
+                    for (int t = 0; t < 4; ++t)
+                        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[t] << 16)),
+                                           fabsf(__uint_as_float(w4[t] & 0xffff0000u))));
+                }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1)
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                int e = 0;
+                if (m > 0.f && isfinite(m)) {
+                    int x;
+                    frexpf(m, &x);
+                    e = min(120, max(-120, 14 - x));
+                }
+                const float f = exp2i(e);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int c = 4 * warp + ((t + lane) & 3);  // 8-d chunk: d = 8c .. 8c+7
+                    const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * c);
+                    const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+                    uint32_t hv[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        hv[u] = pack_half2(__uint_as_float(w4[u] << 16) * f, __uint_as_float(w4[u] & 0xffff0000u) * f);
+                    *reinterpret_cast<uint4 *>(qh + core_off(lane, 8 * c, C::Q_SR, C::Q_SC)) =
+                        make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                }
+                if (warp == 0 && lane == 0)
+                    cred[4 + (piece & 1)] = a.q_scale_log2 * exp2i(-e);  // log2-domain factor of raw scores
+                __syncwarp();
                 if (lane == 0)
-                    red[warp * 16 + j] = m;
+                    mbar_arrive(qfree);  // this warp has read the raw Q
+                // the next piece's Q, once every warp has read this one (only if this CTA has it)
+                const int i_next = i + (cur.nblk - cur.blk);
+                if (warp == 0 && i_next < n) {
+                    Cursor nx = cur;
+                    nx.blk = cur.nblk - 1;
+                    cursor_next(nx, a, groups);
+                    if (!__all_sync(0xffffffffu, wait_phase(qfree, (uint32_t)piece & 1u, abort_flag)))
+                        break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(qfull, NH * D * 2);
+                        bulk_load(qraw, a.q + ((size_t)nx.b * a.num_q_heads + nx.g * NH) * D, NH * D * 2, qfull);
+                    }
+                    ++q_issued;
+                }
             }
-            float vm = valid ? vsv : 0.f;
+            // ---- this token's K and V codes, every chunk loaded before any store
+            uint4 kc[D / 16], vc[D / 16];
+            {
+                const uint8_t *krow = st + tok * D;
+                const uint8_t *vrow = st + C::CODES + tok * D;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                for (int j = 0; j < D / 16; ++j) {
+                    const uint32_t so = (uint32_t)(j ^ (tok & 7)) << 4;
+                    kc[j] = *reinterpret_cast<const uint4 *>(krow + so);
+                    vc[j] = *reinterpret_cast<const uint4 *>(vrow + so);
+                }
+            }
+            {
+                const int pos = (cur.t_first + 2 * cur.blk) * kTileTokens + tok;
+                const bool valid = box_ok[r * C::BOXES + (tok >> 4)] != 0 && pos >= cur.lo && pos < cur.L;
+                float *scb = sc + buf * 3 * BT;
+                scb[tok] = ksr[0];
+                scb[BT + tok] = vsr[0];
+                scb[2 * BT + tok] = valid ? 1.f : 0.f;
+            }
+            // ---- K: 128 codes -> fp16 pairs in tensor memory (lane tok, 64 columns)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t kr[32];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const uint4 kv = kc[4 * half + jj];
+                    i8x4_to_f16x2x2(kv.x, kr[8 * jj + 0], kr[8 * jj + 1]);
+                    i8x4_to_f16x2x2(kv.y, kr[8 * jj + 2], kr[8 * jj + 3]);
+                    i8x4_to_f16x2x2(kv.z, kr[8 * jj + 4], kr[8 * jj + 5]);
+                    i8x4_to_f16x2x2(kv.w, kr[8 * jj + 6], kr[8 * jj + 7]);
+                }
+                tmem_st32(tmem + lane_base + C::K_COL + (uint32_t)buf * 64 + 32 * half, kr);
+            }
+            tmem_wait_st();
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
             if (lane == 0)
-                red[128 + warp] = vm;
-            __syncthreads();
-            float vmax = red[128];
+                mbar_arrive(kready + buf);
+            // ---- V: fp16 in place over this warp's 8 KB of codes in stage r (every lane's
+            // rows are in registers once the warp passes the barrier): the MN-major A operand
+            // of O^T += V^T P', token group g = lane / 8 of the warp at (g < 2 ? K half :
+            // V half) + 4096 warp + 2048 (g % 2), row lane % 8 of its 16 core matrices.
+            __syncwarp();
+            {
+                const int g = lane >> 3;
+                uint8_t *vb = st + (g >> 1) * C::CODES + warp * 4096 + (g & 1) * 2048 + (lane & 7) * 16;
 #pragma unroll
-            for (int k = 1; k < 8; ++k)
-                vmax = fmaxf(vmax, red[128 + k]);
-            const int E_new = max(E_run, ceil_log2_pow(vmax));
-            const int dE = E_run - E_new;
-            const float escale = dE < -126 ? 0.f : exp2i(dE);
-            float fo[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float bm = red[(4 * hh) * 16 + j];
-#pragma unroll
-                for (int k = 1; k < 4; ++k)
-                    bm = fmaxf(bm, red[(4 * hh + k) * 16 + j]);
-                const float mn = fmaxf(m_ref[j], bm);
-                const float fl = (mn == -INFINITY) ? 1.f : fast_exp2((m_ref[j] - mn) * gh);
-                l_acc[j] *= fl;
-                fo[j] = fl * escale;
-                m_ref[j] = mn;
-                dd[j] = valid ? fmaf(y[j], gh, -mn * gh) : -INFINITY;
+                for (int j = 0; j < D / 16; ++j) {
+                    uint32_t v8[8];
+                    i8x4_to_f16x2x2(vc[j].x, v8[0], v8[1]);
+                    i8x4_to_f16x2x2(vc[j].y, v8[2], v8[3]);
+                    i8x4_to_f16x2x2(vc[j].z, v8[4], v8[5]);
+                    i8x4_to_f16x2x2(vc[j].w, v8[6], v8[7]);
+                    *reinterpret_cast<uint4 *>(vb + (2 * j) * C::V_SC) = make_uint4(v8[0], v8[1], v8[2], v8[3]);
+                    *reinterpret_cast<uint4 *>(vb + (2 * j + 1) * C::V_SC) = make_uint4(v8[4], v8[5], v8[6], v8[7]);
+                }
             }
-            E_run = E_new;
-            if (o_valid) {
-                // O^T row tok (a d index), columns = heads 16hh..16hh+15
-                uint32_t orr[16];
-                tmem_ld16(tmem + tl + O_COL + 16 * hh, orr);
+            // vready[buf] may take block i's arrivals only once the MMA thread has consumed
+            // block i-2's phase (O^T(i-2) done): else its wait on that phase could be lapped
+            if (i >= 2 && !__all_sync(0xffffffffu, wait_phase(odone + buf, ph2(i - 2), abort_flag))) {
+                ++i;
+                break;
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(vready + buf);
+            // ---- scales of this thread's token in block n_issued (its codes come from the TMA warp)
+#pragma unroll
+            for (int j = 0; j + 1 < RING; ++j) {
+                ksr[j] = ksr[j + 1];
+                vsr[j] = vsr[j + 1];
+            }
+            ksr[RING - 1] = vsr[RING - 1] = 0.f;
+            if (n_issued < n) {
+                load_token_scales(a, pre, tok, idn, ksr[RING - 1], vsr[RING - 1]);
+                cursor_next(pre, a, groups);
+                ++n_issued;
+            }
+            cursor_next(cur, a, groups);
+        }
+        if (*abort_flag && lane == 0 && warp == 0 && q_issued > piece + 1)
+            mbar_wait_bounded(qfull, (uint32_t)(q_issued - 1) & 1u);  // the Q copy still in flight (bounded)
+    } else if (warp == 9) {
+        // ================================================================ TMA producer
+        // ring stage j % RING takes block j once O^T of block j - RING has read its V;
+        // lane 4t + c fetches the block id of box c of tile t a block ahead
+        if (lane == 0) {
+            const bool p64 = a.page_size == kTileTokens;
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.k_map64 : &a.k_map))
+                         : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.v_map64 : &a.v_map))
+                         : "memory");
+        }
+        Cursor pre = c0;
+        int32_t idc = lane < 8 ? fetch_tile_box_id(a, pre, lane >> 2, lane & 3) : kNoBlock;
+        int j = 0;
+        for (; j < n; ++j) {
+            const int r = j % RING;
+            if (j >= RING &&
+                !__all_sync(0xffffffffu, wait_phase(tfree + r, (uint32_t)(j / RING - 1) & 1u, abort_flag)))
+                break;
+            Cursor nx = pre;
+            cursor_next(nx, a, groups);
+            const int32_t id_next = (lane < 8 && j + 1 < n) ? fetch_tile_box_id(a, nx, lane >> 2, lane & 3) : kNoBlock;
+            issue_block(a, pre, lane, idc, base + C::OFF_RING + r * C::STAGE, tfull + 2 * r, box_ok + r * C::BOXES);
+            idc = id_next;
+            pre = nx;
+        }
+        if (*abort_flag && lane == 0) {
+            // let the copies still in flight land before the CTA leaves (bounded): the last
+            // block issued into each stage
+            for (int jj = max(0, j - RING); jj < j; ++jj)
+                for (int t = 0; t < 2; ++t)
+                    mbar_wait_bounded(tfull + 2 * (jj % RING) + t, (uint32_t)(jj / RING) & 1u);
+        }
+    } else if (warp == 8) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            // descriptors of the shared-memory operands at their buffers' starts
+            const uint64_t qdesc0 = umma_sdesc(smem_u32(qh), C::Q_SC, C::Q_SR);
+            const uint64_t vdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING), C::V_SR, C::V_SC);
+            const uint64_t pdesc0 = umma_sdesc(smem_u32(ph), C::P_SR, C::P_SC);
+            Cursor cur = c0;
+            int n_qk = 0, n_pv = 0, piece = -1;
+            uint32_t first_bits = 0;  // bit (j & 31): block j starts a piece
+            bool ok = true;
+            for (int i = 0; i < n && ok; ++i) {
+                const int buf = i & 1;
+                if (i == 0 || cur.blk == 0)
+                    first_bits |= 1u << (i & 31);
+                else
+                    first_bits &= ~(1u << (i & 31));
+                // S^T(i) = K(i) Q^T: K from tensor memory, Q from shared memory.  The
+                // S buffer [buf] was read by softmax(i-2), waited for before O^T(i-2).
+                if (!wait_phase(kready + buf, ph2(i), abort_flag))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_f16_ts(tmem + C::S_COL + (uint32_t)buf * NH, tmem + C::K_COL + (uint32_t)buf * 64 + 8 * kk,
+                                desc_add(qdesc0, kk * 2 * C::Q_SC), IDESC_QK, kk > 0);
+                umma_commit(sfull + buf);
+                ++n_qk;
+                if (i >= 1)
+                    ok = issue_pv(i - 1, first_bits, piece, n_pv, tmem, vdesc0, pdesc0, pready, vready, ofree, odone,
+                                  tfree, abort_flag);
+                cursor_next(cur, a, groups);
+            }
+            if (ok && n_qk == n)
+                issue_pv(n - 1, first_bits, piece, n_pv, tmem, vdesc0, pdesc0, pready, vready, ofree, odone, tfree,
+                         abort_flag);
+            if (*abort_flag) {
+                // let the tensor core finish what was issued (bounded)
+                if (n_qk > 0)
+                    mbar_wait_bounded(sfull + ((n_qk - 1) & 1), ph2(n_qk - 1));
+                if (n_pv > 0)
+                    mbar_wait_bounded(odone + ((n_pv - 1) & 1), ph2(n_pv - 1));
+            }
+        }
+    } else {
+        // ================================================================ softmax
+        const int sw = warp - 4, tok = tid - 128;
+        // per head: this token's sum of p.  The reference maxima (log2 domain),
+        // the same in every softmax thread, live in mref (shared memory).
+        float l_acc[NH];
+        int E_run = -100;         // running power-of-two bound of the V scales
+        float gh = 0.f;           // log2-domain factor of the raw scores of the piece
+        int piece = -1, piece_first_i = 0;
+        bool piece_from_start = false;
+        Cursor cur = c0;
+        for (int i = 0; i < n; ++i) {
+            const int buf = i & 1;
+            const bool first = (i == 0) || cur.blk == 0;
+            const bool last = (i == n - 1) || cur.blk == cur.nblk - 1;
+            if (first) {
+                ++piece;
+                piece_first_i = i;
+                piece_from_start = cur.blk == 0;
+                E_run = -100;
+#pragma unroll
+                for (int j = 0; j < NH; ++j)
+                    l_acc[j] = 0.f;
+            }
+            bool ok = wait_phase(kready + buf, ph2(i), abort_flag);
+            // the scales (and the piece's Q factor) are in place once K(i) is
+            const float *scb = sc + buf * 3 * BT;
+            const float ksv = scb[tok], vsv = scb[BT + tok];
+            const bool valid = scb[2 * BT + tok] != 0.f;
+            if (first)
+                gh = cred[4 + (piece & 1)];
+            float mr[NH];  // the reference maxima, kept in registers while they hold
+            if (!first) {
+#pragma unroll
+                for (int q = 0; q < NH / 4; ++q) {
+                    const float4 m4 = reinterpret_cast<const float4 *>(mref)[q];
+                    mr[4 * q] = m4.x;
+                    mr[4 * q + 1] = m4.y;
+                    mr[4 * q + 2] = m4.z;
+                    mr[4 * q + 3] = m4.w;
+                }
+            }
+            ok = ok && wait_phase(sfull + buf, ph2(i), abort_flag);
+            tc_fence_after();
+            uint32_t sr[NH];
+            {
+                uint32_t s0[16], s1[16];
+                tmem_ld16(tmem + lane_base + C::S_COL + (uint32_t)buf * NH, s0);
+                tmem_ld16(tmem + lane_base + C::S_COL + (uint32_t)buf * NH + 16, s1);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    orr[j] = __float_as_uint(__uint_as_float(orr[j]) * fo[j]);
-                tmem_st16(tmem + tl + O_COL + 16 * hh, orr);
-                tmem_wait_st();
+                for (int j = 0; j < 16; ++j) {
+                    sr[j] = s0[j];
+                    sr[16 + j] = s1[j];
+                }
             }
-        }
-        // ---- P' = 2^dd * s_v * 2^(6-E) as fp16 row tok of P (heads 16hh..16hh+15)
-        const float vf = valid ? vsv * exp2i(6 - E_run) : 0.f;
-        uint32_t pk[8];
+            const float kg = ksv * gh;  // raw score -> log2 domain
+            // a piece's first block always moves the references (they start at -inf)
+            bool need = valid && (first || !(vsv <= exp2i(E_run)));
+            if (!first) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float p0 = fast_exp2(dd[2 * k]), p1 = fast_exp2(dd[2 * k + 1]);
-            l_acc[2 * k] += p0;
-            l_acc[2 * k + 1] += p1;
-            pk[k] = pack_half2(p0 * vf, p1 * vf);
-        }
-        *reinterpret_cast<uint4 *>(ph + core_off(tok, 16 * hh, C::P_SR, C::P_SC)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4 *>(ph + core_off(tok, 16 * hh + 8, C::P_SR, C::P_SC)) =
-            make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();  // B3: P' ready (and any O rescale done)
-        if (*flag)
-            break;
-        tc_fence_after();
-        // ---- O^T += V^T P' on the tensor cores (A = V, B = P', both MN-major)
-        if (tid == 0) {
+                for (int j = 0; j < NH; ++j)
+                    need |= valid && !(fmaf(__uint_as_float(sr[j]), kg, -mr[j]) <= 8.f);
+            }
+            if (named_bar_or(BAR_SM, 128, need || !ok)) {
+                if (named_bar_or(BAR_SM, 128, !ok))
+                    break;  // abort (every softmax thread leaves here together)
+                // rare: move the references to the block maxima (and the V-scale bound)
+                {
+                    float mv[NH];
 #pragma unroll
-            for (int kk = 0; kk < C::BT / 16; ++kk)
-                umma_f16(tmem + O_COL, umma_sdesc(vh_u + kk * 2 * C::KV_SR, C::KV_SR, C::KV_SC),
-                         umma_sdesc(ph_u + kk * 2 * C::P_SR, C::P_SR, C::P_SC), IDESC_PV, o_valid || kk > 0);
-            umma_commit(mbar_o);
+                    for (int j = 0; j < NH; ++j)
+                        mv[j] = valid ? __uint_as_float(sr[j]) * kg : -INFINITY;
+                    red[sw * NH + lane] = warp_transpose_reduce<true>(mv, lane);  // head lane's warp maximum
+                }
+                float vm = valid ? vsv : 0.f;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                if (lane == 0)
+                    red[4 * NH + sw] = vm;
+                named_bar(BAR_SM, 128);
+                const float vmax = fmaxf(fmaxf(red[4 * NH], red[4 * NH + 1]), fmaxf(red[4 * NH + 2], red[4 * NH + 3]));
+                const int E_new = max(E_run, ceil_log2_pow(vmax));
+                const int dE = E_run - E_new;
+                const float escale = dE < -126 ? 0.f : exp2i(dE);
+                // thread tok < 32 moves head tok's reference; every thread rescales its l
+                if (tok < NH) {
+                    const float bm = fmaxf(fmaxf(red[tok], red[NH + tok]), fmaxf(red[2 * NH + tok], red[3 * NH + tok]));
+                    const float mo = first ? -INFINITY : mref[tok];
+                    const float mn = fmaxf(mo, bm);
+                    const float fl = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
+                    mref[tok] = mn;
+                    ofac_s[tok] = fl;
+                }
+                named_bar(BAR_SM, 128);
+#pragma unroll
+                for (int j = 0; j < NH; ++j)
+                    l_acc[j] *= ofac_s[j];
+                E_run = E_new;
+                if (!first) {
+                    // O of this piece, once O^T(i-1) has landed: row d = tok, 32 heads
+                    wait_phase(odone + ((i - 1) & 1), ph2(i - 1), abort_flag);
+                    tc_fence_after();
+                    const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH;
+#pragma unroll
+                    for (int hq = 0; hq < 2; ++hq) {
+                        uint32_t orr[16];
+                        tmem_ld16(tmem + lane_base + o_col + 16 * hq, orr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            orr[j] = __float_as_uint(__uint_as_float(orr[j]) * (ofac_s[16 * hq + j] * escale));
+                        tmem_st16(tmem + lane_base + o_col + 16 * hq, orr);
+                    }
+                    tmem_wait_st();
+                }
+                named_bar(BAR_SM, 128);  // reductions read before red is reused
+#pragma unroll
+                for (int q = 0; q < NH / 4; ++q) {
+                    const float4 m4 = reinterpret_cast<const float4 *>(mref)[q];
+                    mr[4 * q] = m4.x;
+                    mr[4 * q + 1] = m4.y;
+                    mr[4 * q + 2] = m4.z;
+                    mr[4 * q + 3] = m4.w;
+                }
+            }
+            // ---- P' = 2^(score - ref) * s_v * 2^(6-E) as fp16 row tok of P'[buf]
+            if (i >= 2)  // P' buffer [buf] free once O^T(i-2) is done
+                wait_phase(odone + buf, ph2(i - 2), abort_flag);
+            const float vf = valid ? vsv * exp2i(6 - E_run) : 0.f;
+            uint8_t *pb = ph + buf * BT * NH * 2;
+#pragma unroll
+            for (int q = 0; q < NH / 8; ++q) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j0 = 8 * q + 2 * k;
+                    const float p0 = valid ? fast_exp2(fmaf(__uint_as_float(sr[j0]), kg, -mr[j0])) : 0.f;
+                    const float p1 = valid ? fast_exp2(fmaf(__uint_as_float(sr[j0 + 1]), kg, -mr[j0 + 1])) : 0.f;
+                    l_acc[j0] += p0;
+                    l_acc[j0 + 1] += p1;
+                    pk[k] = pack_half2(p0 * vf, p1 * vf);
+                }
+                *reinterpret_cast<uint4 *>(pb + core_off(tok, 8 * q, C::P_SR, C::P_SC)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(pready + buf);
+            if (last) {
+                // ---- epilogue of the piece: l per head over the 128 token rows, normalise O
+                wait_phase(odone + buf, ph2(i), abort_flag);  // O^T(i) landed
+                tc_fence_after();
+                {
+                    float lv[NH];
+#pragma unroll
+                    for (int j = 0; j < NH; ++j)
+                        lv[j] = l_acc[j];
+                    red[sw * NH + lane] = warp_transpose_reduce<false>(lv, lane);  // head lane's warp sum
+                }
+                const bool whole_pair = piece_from_start && cur.blk == cur.nblk - 1;
+                const int slot = piece_first_i == 0 ? 0 : 1;
+                named_bar(BAR_SM, 128);
+                if (tok < NH) {
+                    // head tok: l, the output factor 2^(E-6) / l and (for a partial) the lse
+                    const float l = red[tok] + red[NH + tok] + red[2 * NH + tok] + red[3 * NH + tok];
+                    ofac_s[tok] = l > 0.f ? __fdividef(exp2i(E_run - 6), l) : 0.f;
+                    if (!whole_pair && cur.g * NH + tok < a.num_q_heads)
+                        a.lse[(size_t)(2 * cta + slot) * NH + tok] =
+                            l > 0.f ? (mref[tok] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                }
+                const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH;
+                uint32_t ov[NH];
+                {
+                    uint32_t o0[16], o1[16];
+                    tmem_ld16(tmem + lane_base + o_col, o0);
+                    tmem_ld16(tmem + lane_base + o_col + 16, o1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        ov[j] = o0[j];
+                        ov[16 + j] = o1[j];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(ofree + (piece & 1));
+                named_bar(BAR_SM, 128);  // ofac_s ready
+                const int nh = min(NH, a.num_q_heads - cur.g * NH);  // heads of this group that exist
+                if (whole_pair) {
+                    __nv_bfloat16 *dst = a.out + ((size_t)cur.b * a.num_q_heads + cur.g * NH) * D + tok;
+#pragma unroll
+                    for (int j = 0; j < NH; ++j)
+                        if (j < nh)
+                            dst[(size_t)j * D] = __float2bfloat16_rn(__uint_as_float(ov[j]) * ofac_s[j]);
+                } else {
+                    float *dst = a.o_partial + (size_t)(2 * cta + slot) * NH * D + tok;
+#pragma unroll
+                    for (int j = 0; j < NH; ++j)
+                        dst[(size_t)j * D] = __uint_as_float(ov[j]) * ofac_s[j];
+                }
+                if (!whole_pair) {
+                    // ticket: the last piece of the pair to finish merges it
+                    __threadfence();
+                    named_bar(BAR_SM, 128);
+                    if (tok == 0) {
+                        const long long g0 = list_first + i - cur.blk, g1 = g0 + cur.nblk - 1;
+                        const int c_lo = cta_of(g0, list_n, Ge), c_hi = cta_of(g1, list_n, Ge);
+                        const int ticket = atomicAdd(a.counters + (size_t)cur.b * groups + cur.g, 1);
+                        if (ticket == c_hi - c_lo) {
+                            const int k = merges[0]++;
+                            int *m = merges + 1 + 5 * k;
+                            m[0] = cur.b;
+                            m[1] = cur.g;
+                            m[2] = c_lo;
+                            m[3] = c_hi;
+                            m[4] = (list_n * c_lo / Ge == g0) ? 0 : 1;  // slot of the pair in CTA c_lo
+                        }
+                    }
+                }
+                named_bar(BAR_SM, 128);  // red is reused by the next piece
+            }
+            cursor_next(cur, a, groups);
         }
-        ++n_pv;
-        o_valid = true;
     }
 
-    const bool timed_out = *flag != 0;
-    if (timed_out) {
-        // a bounded wait ran out: report; let copies and MMAs in flight land (bounded)
-        if (tid == 0) {
-            set_status(a.dev_status, MQA_DEV_TIMEOUT);
-            // only what was issued: each barrier's last phase (an older parity would alias)
-            for (int j = blk; j < n_issued; ++j)
-                for (int w = 0; w < C::BOXES; ++w)
-                    mbar_wait_bounded(mbar + (j % RING) * C::BOXES + w, (uint32_t)(j / RING) & 1u);
-            if (n_qk > 0)
-                mbar_wait_bounded(mbar_s, (uint32_t)(n_qk - 1) & 1u);
-            if (n_pv > 0)
-                mbar_wait_bounded(mbar_o, (uint32_t)(n_pv - 1) & 1u);
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0)
-            tmem_dealloc(tmem, C::TMEM_COLS);
-        return;
-    }
-    if (!mbar_wait_bounded(mbar_o, (uint32_t)(n_blocks - 1) & 1u) && tid == 0)
-        set_status(a.dev_status, MQA_DEV_TIMEOUT);
-    tc_fence_after();
-
-    // ---- epilogue: l per head over the block's 128 token rows, normalise O, store
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        float v = l_acc[j];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0)
-            red[warp * 16 + j] = v;
-    }
-    __syncthreads();
-    uint32_t ov[16];
-    tmem_ld16(tmem + tl + O_COL + 16 * hh, ov);  // O^T row d = tok, heads 16hh..16hh+15
-    tmem_wait_ld();
-    const float ofac = exp2i(E_run - 6);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int h = h0 + 16 * hh + j;
-        if (h >= a.num_q_heads)
-            continue;
-        const float l = red[(4 * hh) * 16 + j] + red[(4 * hh + 1) * 16 + j] + red[(4 * hh + 2) * 16 + j] +
-                        red[(4 * hh + 3) * 16 + j];
-        const float val = l > 0.f ? __uint_as_float(ov[j]) * (ofac / l) : 0.f;
-        if (split_mode) {
-            const size_t rowoff = ((size_t)b * a.num_splits + split) * a.num_q_heads + h;
-            a.o_partial[rowoff * D + tok] = val;
-            if (tok == 0)
-                a.lse[rowoff] = l > 0.f ? (m_ref[j] * gh + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        } else {
-            a.out[((size_t)b * a.num_q_heads + h) * D + tok] = __float2bfloat16_rn(val);
-        }
-    }
+    // ---- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 0)
+    const bool aborted = *abort_flag != 0;
+    if (aborted && tid == 0)
+        set_status(a.dev_status, MQA_DEV_TIMEOUT);
+    if (warp == 8) {
+        tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
-
-    // ---- fused split-KV merge: the last of this sequence's split CTAs merges them
-    if (split_mode && a.counters != nullptr) {
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const int n_active = (t_last - t_first + 1 + a.tiles_per_split - 1) / a.tiles_per_split;
-            const int ticket = atomicAdd(a.counters + (size_t)b * gridDim.z + blockIdx.z, 1);
-            *flag = (ticket == n_active - 1) ? 2 : 0;
-        }
-        __syncthreads();
-        if (*flag == 2 && warp < 4) {
+    }
+    // ---- deferred merges of the pairs whose last piece finished here: thread t of
+    // warps 0-7 merges head t / 8, d = 16 (t % 8) .. +15.  The 8 lanes of a head
+    // load its pieces' lse values together; the weights go through shared memory
+    // (the idle ring); the partial rows stream with 16 loads in flight per thread.
+    if (!aborted && warp < 8) {
+        const int nm = merges[0];
+        if (nm > 0)
             __threadfence();
-            const int n_active = (t_last - t_first + 1 + a.tiles_per_split - 1) / a.tiles_per_split;
-            merge_splits<D, NH>(a, b, h0, n_active);
+        float *wts = reinterpret_cast<float *>(base + C::OFF_RING);  // [32 heads][np]
+        const int jh = tid >> 3, sub = tid & 7, d0 = sub * 16;
+        for (int k = 0; k < nm; ++k) {
+            const int *m = merges + 1 + 5 * k;
+            const int mb = m[0], mgp = m[1], c_lo = m[2], c_hi = m[3], slot_lo = m[4];
+            const int np = c_hi - c_lo + 1;  // <= CTAs of the grid: [32][np] floats fit the ring
+            const int h = mgp * NH + jh;
+            float M = -INFINITY;
+            for (int p = sub; p < np; p += 8)
+                M = fmaxf(M, __ldcg(a.lse + merge_row(c_lo, p, slot_lo, jh)));
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1)
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            float den = 0.f;
+            for (int p = sub; p < np; p += 8) {
+                const float ls = __ldcg(a.lse + merge_row(c_lo, p, slot_lo, jh));
+                const float wv = (ls == -INFINITY || M == -INFINITY) ? 0.f : __expf(ls - M);
+                wts[jh * np + p] = wv;
+                den += wv;
+            }
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1)
+                den += __shfl_xor_sync(0xffffffffu, den, off);
+            __syncwarp();
+            float4 acc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int p0 = 0; p0 < np; p0 += 4) {
+                float4 x[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int p = min(p0 + u, np - 1);
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(a.o_partial + merge_row(c_lo, p, slot_lo, jh) * D + d0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        x[u][q] = __ldcg(src + q);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float wv = p0 + u < np ? wts[jh * np + p0 + u] : 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[q].x += wv * x[u][q].x;
+                        acc[q].y += wv * x[u][q].y;
+                        acc[q].z += wv * x[u][q].z;
+                        acc[q].w += wv * x[u][q].w;
+                    }
+                }
+            }
+            if (h < a.num_q_heads) {
+                const float f = den > 0.f ? 1.f / den : 0.f;
+                uint32_t pk[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    pk[2 * q] = pack_bf16x2(acc[q].x * f, acc[q].y * f);
+                    pk[2 * q + 1] = pack_bf16x2(acc[q].z * f, acc[q].w * f);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)mb * a.num_q_heads + h) * D + d0);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+            __syncwarp();  // wts reused by the next merge
         }
     }
 }
@@ -492,8 +1199,7 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s)
             return e;
         attr_set.store(1, std::memory_order_release);
     }
-    dim3 grid(a.num_splits, a.batch, (a.num_q_heads + TcCfg::NH - 1) / TcCfg::NH);
-    decode_tc_kernel<<<grid, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(a);
+    decode_tc_kernel<<<a.persist_ctas, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -20,7 +20,8 @@ struct AppendArgs {
 cudaError_t launch_quant_append(const AppendArgs &a, cudaStream_t s);
 
 struct DecodeArgs {
-    CUtensorMap k_map, v_map;          // 2-D maps over [num_blocks*page_size, head_dim] int8
+    CUtensorMap k_map, v_map;          // 2-D maps over [num_blocks*page_size, head_dim] int8, 16-row boxes
+    CUtensorMap k_map64, v_map64;      // the same with 64-row boxes (tcgen05 kernel, page_size 64 only)
     const float *k_scale, *v_scale;
     const int32_t *block_table, *seq_lens;
     const __nv_bfloat16 *q;
@@ -32,6 +33,11 @@ struct DecodeArgs {
     int32_t num_q_heads, window;
     int32_t tiles_per_split, num_splits;
     float q_scale_log2;                // sm_scale * log2(e)
+    // tcgen05 kernel only: persistent != 0 = balanced shares of the (sequence,
+    // head group, block) list over persist_ctas CTAs (partials in o_partial /
+    // lse rows [2 * persist_ctas][32], tickets in counters); 0 = one CTA per
+    // (sequence, head group), persist_ctas = batch * head groups
+    int32_t persistent, persist_ctas;
 };
 cudaError_t launch_decode(const DecodeArgs &a, int head_dim, cudaStream_t s);
 // head_dim 128 with 32 or 64 query heads runs on the tcgen05 kernel; the rest on the warp-MMA kernel

@@ -189,6 +189,76 @@ def test_device_checks_flag_bad_inputs_without_faulting():
     assert torch.all(out[1].float() == 0)
 
 
+def test_decode_batch_above_one_pass_partition():
+    """More sequences (300) than the tensor-core kernel's threads: its work
+    partition takes the multi-pass path; ragged short lengths, both windows."""
+    rng = np.random.default_rng(12)
+    lens = rng.integers(1, 700, size=300).astype(np.int32)
+    s = build_caches(rng, lens, 64, 128, 1)
+    for window in (0, 256):
+        q = synth.bf16_normal(rng, (len(lens), 32, 128))
+        out, ref = run_decode(s, q, window, num_splits=0)
+        assert_close(out, ref, f"batch 300 W={window}")
+
+
+@pytest.mark.parametrize("heads", [32, 64])
+def test_decode_one_long_sequence_cut_into_many_pieces(heads):
+    """Batch 1, 40k tokens: the balanced split cuts the sequence into one piece
+    per CTA (far more than 32), all merged by the last one."""
+    rng = np.random.default_rng(13 + heads)
+    lens = np.array([40000], np.int32)
+    s = build_caches(rng, lens, 64, 128, 1)
+    q = synth.bf16_normal(rng, (1, heads, 128))
+    out, ref = run_decode(s, q, 0, num_splits=0)
+    assert_close(out, ref, f"one long sequence H={heads}")
+
+
+def test_back_to_back_calls_keep_every_handoff_in_step():
+    """Many decode calls in a row, alternating a local and a global layer over
+    two caches (the warp-specialised kernel's barriers are exercised hundreds
+    of thousands of times): no call may report a timeout, and the outputs
+    still match the oracle."""
+    rng = np.random.default_rng(15)
+    # the 24-layer workload's length mix: batch 128, lognormal around 4k, many short
+    # sequences (pieces of a single block follow one another)
+    lens = synth.seq_lens_for(synth.CONFIGS["stack24_b128"], rng)
+    s = build_caches(rng, lens, 64, 128, 2)
+    q_bits = synth.bf16_normal(rng, (2, len(lens), 32, 128))
+    qs = [to_dev_bf16(q_bits[i]) for i in range(2)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = {}
+    for it in range(48):
+        layer = it % 2
+        window = 1024 if layer == 0 else 0
+        outs[layer] = mk.mqa_decode_attn(s.gpu_caches, [0, 1], layer, window, s.batch, qs[layer],
+                                         sm_scale=sm_scale(128), num_splits=0, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
+    for layer, window in ((0, 1024), (1, 0)):
+        ref, _ = oracle.decode(s.ora_caches[layer], s.pb.block_table, s.seq_lens, q_bits[layer], window,
+                               sm_scale(128))
+        assert_close(outs[layer], ref, f"back-to-back layer {layer}")
+
+
+def test_device_length_check_in_balanced_mode():
+    """A device length beyond max_seq_len with automatic splitting: that
+    sequence is zero-filled and flagged, the others are computed."""
+    rng = np.random.default_rng(14)
+    lens = np.array([100, 200, 3000], np.int32)
+    s = build_caches(rng, lens, 64, 128, 1)
+    q_bits = synth.bf16_normal(rng, (3, 32, 128))
+    q = to_dev_bf16(q_bits)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev_lens = to_dev_i32(np.array([100, 5000, 3000], np.int32))
+    b2 = mk.Batch(s.batch.block_table, dev_lens, None, 3000)
+    out = mk.mqa_decode_attn(s.gpu_caches, [0], 0, 0, b2, q, num_splits=0, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & mk.MQA_DEV_BAD_SEQLEN
+    assert torch.all(out[1].float() == 0)
+    ref, _ = oracle.decode(s.ora_caches[0], s.pb.block_table, lens, q_bits, 0, sm_scale(128))
+    assert_close(out[[0, 2]], ref[[0, 2]], "balanced mode, valid sequences")
+
+
 # ----------------------------------------------------------------- combine
 @pytest.mark.parametrize("d", [64, 128])
 def test_split_kv_combine_matches_oracle(d):
