@@ -54,6 +54,7 @@ struct TcCfg {
     static constexpr int BT = 128;                   // tokens per block (M of S^T, K of O^T)
     static constexpr int BOXES = BT / kChunkTokens;  // 8 TMA boxes of 16 tokens
     static constexpr int RING = 5;                   // ring stages (codes in flight, then fp16 V)
+    static constexpr int DEPTH = 3;                  // blocks in flight between roles (S, K, P, scales)
     static constexpr int THREADS = 320;              // 4 converter + 4 softmax warps, MMA warp, TMA warp
     static constexpr int CODES = BT * D;             // int8 bytes of K (or V) of a block
     static constexpr int STAGE = 2 * CODES;          // K codes, V codes; then fp16 V in place
@@ -61,19 +62,19 @@ struct TcCfg {
     static constexpr int OFF_RING = 0;
     static constexpr int OFF_QH = OFF_RING + RING * STAGE;      // fp16 Q [32 h][128 d], core layout
     static constexpr int OFF_QRAW = OFF_QH + NH * D * 2;        // bf16 Q [32 h][128 d] as copied (next piece)
-    static constexpr int OFF_PH = OFF_QRAW + NH * D * 2;        // [2] fp16 P' [128 tok][32 h], core layout
-    static constexpr int OFF_SC = OFF_PH + 2 * BT * NH * 2;     // [2][3][128] fp32: K scale, V scale, valid
-    static constexpr int OFF_RED = OFF_SC + 2 * 3 * BT * 4;     // softmax group: [4 warps][32] + [4] fp32
+    static constexpr int OFF_PH = OFF_QRAW + NH * D * 2;        // [DEPTH] fp16 P' [128 tok][32 h], core layout
+    static constexpr int OFF_SC = OFF_PH + DEPTH * BT * NH * 2;  // [DEPTH][3][128] fp32: K scale, V scale, valid
+    static constexpr int OFF_RED = OFF_SC + DEPTH * 3 * BT * 4;  // softmax group: [4 warps][32] + [4] fp32
     static constexpr int OFF_MREF = OFF_RED + 160 * 4;          // softmax group: reference maxima [32], factors [32]
-    static constexpr int OFF_CRED = OFF_MREF + 64 * 4;          // converter group: [4] fp32, gh[2]
+    static constexpr int OFF_CRED = OFF_MREF + 64 * 4;          // converter group: [4] fp32, gh[4]
     static constexpr int OFF_OK = OFF_CRED + 16 * 4;            // [RING][8] box arrived
     static constexpr int OFF_MISC = OFF_OK + RING * BOXES * 4;  // tmem base, abort flag, start, merges
     static constexpr int OFF_MBAR = OFF_MISC + 256;
-    static constexpr int NBAR = 4 * RING + 14;  // tile full / free [RING][2] each, 6 x 2 hand-offs, Q full / free
+    static constexpr int NBAR = 4 * RING + 5 * DEPTH + 4;  // tiles, 5 x DEPTH hand-offs, O free [2], Q full / free
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
-    // tensor memory columns: S^T [2][32], O^T [2][32], fp16 K [2][64]
-    static constexpr uint32_t TMEM_COLS = 256;
-    static constexpr uint32_t S_COL = 0, O_COL = 64, K_COL = 128;
+    // tensor memory columns: S^T [DEPTH][32], O^T [2][32], fp16 K [DEPTH][64]
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 0, O_COL = DEPTH * NH, K_COL = O_COL + 2 * NH;
     // core-matrix strides (bytes): V rows = tokens, Q rows = heads, P rows = tokens.  The fp16
     // V of converter warp w's tokens 32w .. 32w+31 overwrites the 8 KB of codes they came
     // from: 8-token groups 0, 1 of the warp at K-half offset 4096w, groups 2, 3 at V-half
@@ -86,6 +87,7 @@ struct TcCfg {
     static constexpr uint32_t P_SC = 128;       // next 8 heads
 };
 static_assert(TcCfg::SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(TcCfg::K_COL + TcCfg::DEPTH * 64 <= TcCfg::TMEM_COLS, "tensor memory budget");
 
 // Mbarrier wait with a suspend hint: a waiting warp sleeps until the phase
 // completes instead of polling (eight warps polling would crowd the shared-
@@ -143,6 +145,9 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool pred)
 
 // Parity of the phase of a two-buffer hand-off barrier that carries item i.
 __device__ __forceinline__ uint32_t ph2(int i) { return (uint32_t)(i >> 1) & 1u; }
+// Buffer and phase parity of block i on a DEPTH-buffer hand-off (i >= 0).
+__device__ __forceinline__ int bufd(int i) { return i % TcCfg::DEPTH; }
+__device__ __forceinline__ uint32_t phd(int i) { return (uint32_t)(i / TcCfg::DEPTH) & 1u; }
 
 // Reduce 32 per-head values over the 32 lanes of a warp with 31 shuffles (a
 // butterfly that halves the values each lane keeps at every step): lane L
@@ -330,8 +335,8 @@ __device__ __forceinline__ bool issue_pv(int j, uint32_t first_bits, int &piece,
 {
     using C = TcCfg;
     constexpr uint32_t IDESC_PV = umma_idesc_f16(128, C::NH, true, true);
-    const int jb = j & 1;
-    if (!wait_phase(pready + jb, ph2(j), abort_flag) || !wait_phase(vready + jb, ph2(j), abort_flag))
+    const int jb = bufd(j);
+    if (!wait_phase(pready + jb, phd(j), abort_flag) || !wait_phase(vready + jb, phd(j), abort_flag))
         return false;
     const bool first = (first_bits >> (j & 31)) & 1u;
     if (first) {
@@ -394,12 +399,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     static_assert(32 + 3 * 8 <= 64 && 64 + 11 * 4 <= 256, "misc layout");
     uint64_t *tfull = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][2] tile codes landed (TMA)
     uint64_t *tfree = tfull + 2 * RING;         // [RING] stage free: O^T of its block done (tensor core)
-    uint64_t *kready = tfree + 2 * RING;        // [2] K in tensor memory, scales, Q   (4 converter warps)
-    uint64_t *vready = kready + 2;              // [2] fp16 V in shared memory          (4 converter warps)
-    uint64_t *pready = vready + 2;              // [2] P' written, S read               (4 softmax warps)
-    uint64_t *sfull = pready + 2;               // [2] S^T = K Q^T done                 (tensor core)
-    uint64_t *odone = sfull + 2;                // [2] O^T += V^T P' done               (tensor core)
-    uint64_t *ofree = odone + 2;                // [2] a piece's O read by its epilogue (4 softmax warps)
+    uint64_t *kready = tfree + 2 * RING;        // [DEPTH] K in tensor memory, scales, Q (4 converter warps)
+    uint64_t *vready = kready + C::DEPTH;       // [DEPTH] fp16 V in shared memory     (4 converter warps)
+    uint64_t *pready = vready + C::DEPTH;       // [DEPTH] P' written, S read          (4 softmax warps)
+    uint64_t *sfull = pready + C::DEPTH;        // [DEPTH] S^T = K Q^T done            (tensor core)
+    uint64_t *odone = sfull + C::DEPTH;         // [DEPTH] O^T += V^T P' done          (tensor core)
+    uint64_t *ofree = odone + C::DEPTH;         // [2] a piece's O read by its epilogue (4 softmax warps)
     uint64_t *qfull = ofree + 2;                // raw Q of the next piece landed      (bulk copy)
     uint64_t *qfree = qfull + 1;                // raw Q read by every converter warp  (4 converter warps)
 
@@ -575,14 +580,15 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             mbar_init(tfull + s, 1);
             mbar_init(tfree + s, 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::DEPTH; ++s) {
             mbar_init(kready + s, 4);
             mbar_init(vready + s, 4);
             mbar_init(pready + s, 4);
             mbar_init(sfull + s, 1);
             mbar_init(odone + s, 1);
-            mbar_init(ofree + s, 4);
         }
+        for (int s = 0; s < 2; ++s)
+            mbar_init(ofree + s, 4);
         mbar_init(qfull, 1);
         mbar_init(qfree, 4);
         *abort_flag = 0;
@@ -634,21 +640,21 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         int piece = -1;
         int i = 0;
         for (; i < n; ++i) {
-            const int r = i % RING, buf = i & 1;
+            const int r = i % RING, buf = bufd(i);
             uint8_t *st = base + C::OFF_RING + r * C::STAGE;
             const bool first = (i == 0) || cur.blk == 0;
             if (n_issued < n)  // used by this iteration's scale loads
                 idn = fetch_tile_box_id(a, pre, tok >> 6, (tok >> 4) & 3);
             bool ok = wait_phase(tfull + 2 * r + my_tile, (uint32_t)(i / RING) & 1u, abort_flag);
-            if (i >= 2) {
-                // K buffer [buf] free once S^T(i-2) is done; scale slot [buf] once softmax(i-2) is
-                ok = ok && wait_phase(sfull + buf, ph2(i - 2), abort_flag);
-                ok = ok && wait_phase(pready + buf, ph2(i - 2), abort_flag);
+            if (i >= C::DEPTH) {
+                // K buffer [buf] free once S^T(i-DEPTH) is done; scale slot [buf] once softmax(i-DEPTH) is
+                ok = ok && wait_phase(sfull + buf, phd(i - C::DEPTH), abort_flag);
+                ok = ok && wait_phase(pready + buf, phd(i - C::DEPTH), abort_flag);
             }
             if (first) {
                 ok = ok && wait_phase(qfull, (uint32_t)(piece + 1) & 1u, abort_flag);  // this piece's raw Q
                 if (i >= 1)  // fp16 Q is single-buffered: every S^T(i-1) must be done
-                    ok = ok && wait_phase(sfull + ((i - 1) & 1), ph2(i - 1), abort_flag);
+                    ok = ok && wait_phase(sfull + bufd(i - 1), phd(i - 1), abort_flag);
             }
             if (!__all_sync(0xffffffffu, ok))
                 break;
@@ -692,7 +698,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                         make_uint4(hv[0], hv[1], hv[2], hv[3]);
                 }
                 if (warp == 0 && lane == 0)
-                    cred[4 + (piece & 1)] = a.q_scale_log2 * exp2i(-e);  // log2-domain factor of raw scores
+                    cred[4 + (piece & 3)] = a.q_scale_log2 * exp2i(-e);  // log2-domain factor of raw scores
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(qfree);  // this warp has read the raw Q
@@ -771,8 +777,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 }
             }
             // vready[buf] may take block i's arrivals only once the MMA thread has consumed
-            // block i-2's phase (O^T(i-2) done): else its wait on that phase could be lapped
-            if (i >= 2 && !__all_sync(0xffffffffu, wait_phase(odone + buf, ph2(i - 2), abort_flag))) {
+            // block i-DEPTH's phase (O^T(i-DEPTH) done): else its wait on that phase could be lapped
+            if (i >= C::DEPTH && !__all_sync(0xffffffffu, wait_phase(odone + buf, phd(i - C::DEPTH), abort_flag))) {
                 ++i;
                 break;
             }
@@ -841,14 +847,14 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             uint32_t first_bits = 0;  // bit (j & 31): block j starts a piece
             bool ok = true;
             for (int i = 0; i < n && ok; ++i) {
-                const int buf = i & 1;
+                const int buf = bufd(i);
                 if (i == 0 || cur.blk == 0)
                     first_bits |= 1u << (i & 31);
                 else
                     first_bits &= ~(1u << (i & 31));
                 // S^T(i) = K(i) Q^T: K from tensor memory, Q from shared memory.  The
                 // S buffer [buf] was read by softmax(i-2), waited for before O^T(i-2).
-                if (!wait_phase(kready + buf, ph2(i), abort_flag))
+                if (!wait_phase(kready + buf, phd(i), abort_flag))
                     break;
                 tc_fence_after();
 #pragma unroll
@@ -868,9 +874,9 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             if (*abort_flag) {
                 // let the tensor core finish what was issued (bounded)
                 if (n_qk > 0)
-                    mbar_wait_bounded(sfull + ((n_qk - 1) & 1), ph2(n_qk - 1));
+                    mbar_wait_bounded(sfull + bufd(n_qk - 1), phd(n_qk - 1));
                 if (n_pv > 0)
-                    mbar_wait_bounded(odone + ((n_pv - 1) & 1), ph2(n_pv - 1));
+                    mbar_wait_bounded(odone + bufd(n_pv - 1), phd(n_pv - 1));
             }
         }
     } else {
@@ -885,7 +891,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         bool piece_from_start = false;
         Cursor cur = c0;
         for (int i = 0; i < n; ++i) {
-            const int buf = i & 1;
+            const int buf = bufd(i);
             const bool first = (i == 0) || cur.blk == 0;
             const bool last = (i == n - 1) || cur.blk == cur.nblk - 1;
             if (first) {
@@ -897,13 +903,13 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 for (int j = 0; j < NH; ++j)
                     l_acc[j] = 0.f;
             }
-            bool ok = wait_phase(kready + buf, ph2(i), abort_flag);
+            bool ok = wait_phase(kready + buf, phd(i), abort_flag);
             // the scales (and the piece's Q factor) are in place once K(i) is
             const float *scb = sc + buf * 3 * BT;
             const float ksv = scb[tok], vsv = scb[BT + tok];
             const bool valid = scb[2 * BT + tok] != 0.f;
             if (first)
-                gh = cred[4 + (piece & 1)];
+                gh = cred[4 + (piece & 3)];  // 4 slots: the converters run up to DEPTH blocks ahead
             float mr[NH];  // the reference maxima, kept in registers while they hold
             if (!first) {
 #pragma unroll
@@ -915,7 +921,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     mr[4 * q + 3] = m4.w;
                 }
             }
-            ok = ok && wait_phase(sfull + buf, ph2(i), abort_flag);
+            ok = ok && wait_phase(sfull + buf, phd(i), abort_flag);
             tc_fence_after();
             uint32_t sr[NH];
             {
@@ -975,7 +981,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 E_run = E_new;
                 if (!first) {
                     // O of this piece, once O^T(i-1) has landed: row d = tok, 32 heads
-                    wait_phase(odone + ((i - 1) & 1), ph2(i - 1), abort_flag);
+                    wait_phase(odone + bufd(i - 1), phd(i - 1), abort_flag);
                     tc_fence_after();
                     const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH;
 #pragma unroll
@@ -1001,8 +1007,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 }
             }
             // ---- P' = 2^(score - ref) * s_v * 2^(6-E) as fp16 row tok of P'[buf]
-            if (i >= 2)  // P' buffer [buf] free once O^T(i-2) is done
-                wait_phase(odone + buf, ph2(i - 2), abort_flag);
+            if (i >= C::DEPTH)  // P' buffer [buf] free once O^T(i-DEPTH) is done
+                wait_phase(odone + buf, phd(i - C::DEPTH), abort_flag);
             const float vf = valid ? vsv * exp2i(6 - E_run) : 0.f;
             uint8_t *pb = ph + buf * BT * NH * 2;
 #pragma unroll
@@ -1027,7 +1033,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 mbar_arrive(pready + buf);
             if (last) {
                 // ---- epilogue of the piece: l per head over the 128 token rows, normalise O
-                wait_phase(odone + buf, ph2(i), abort_flag);  // O^T(i) landed
+                wait_phase(odone + buf, phd(i), abort_flag);  // O^T(i) landed
                 tc_fence_after();
                 {
                     float lv[NH];
