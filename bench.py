@@ -550,8 +550,8 @@ def run_decode(args, w):
                    "kv_bytes_per_step": kv_bytes, "kv_gbps": kv_bytes / (ms * 1e6)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "decode attention call (memset of the merge tickets + the decode kernel, split "
-                               "merge fused), each call timed alone with L2 flushed before it",
+                     "kernel": "decode attention call (the decode kernel + the kernel merging pairs cut between "
+                               "CTAs), each call timed alone with L2 flushed before it",
                      "local": part(loc), "global": part(glo)},
         "eager_ms_per_step": statistics.mean(eager),
         "gpu_launches": stack.launches_per_step() * args.steps,

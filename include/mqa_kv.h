@@ -141,10 +141,13 @@ int mqa_decode_auto_splits(const mqa_batch *batch, int32_t window, int32_t num_q
 
 /* Bytes of decode workspace for `num_splits` splits: fp32 partial outputs
  * [batch][num_splits][num_q_heads][head_dim], then fp32 log-sum-exps
- * [batch][num_splits][num_q_heads], then one int32 ticket per (sequence, group
- * of 32 heads), each region 256-byte aligned.  0 when num_splits <= 1.  With
- * at most 16 splits the decode kernel merges the partials itself (the tickets
- * are zeroed on the stream first); wider splits run split_kv_combine. */
+ * [batch][num_splits][num_q_heads], then max(one int32 ticket per (sequence,
+ * group of 32 heads), 64 KiB of merge descriptors), each region 256-byte
+ * aligned.  0 when num_splits <= 1.  head_dim 128 with 32 or 64 heads runs the
+ * tcgen05 kernel, which writes its partials and merge descriptors there and
+ * merges them in a second kernel; otherwise with at most 16 splits the decode
+ * kernel merges the partials itself (the tickets are zeroed on the stream
+ * first), and wider splits run split_kv_combine. */
 size_t mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t head_dim, int32_t num_splits);
 
 /* Merge split-KV partial results (flash-decoding combine; the same log-sum-exp

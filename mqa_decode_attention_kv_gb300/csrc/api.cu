@@ -156,7 +156,10 @@ int tiles_for(int L, int W)
 int tc_max_ctas(int head_dim, int heads)
 {
     const int sms = sm_count();
-    return sms <= 0 ? 0 : sms * ctas_per_sm(head_dim, heads);
+    if (sms <= 0)
+        return 0;
+    const int g = sms * ctas_per_sm(head_dim, heads);
+    return g < kTcMaxCtas ? g : kTcMaxCtas;
 }
 
 int tc_auto_splits(int batch, int heads, int head_dim)
@@ -316,8 +319,10 @@ size_t mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t hea
 {
     if (num_splits <= 1 || batch <= 0 || num_q_heads <= 0 || head_dim <= 0)
         return 0;
-    return counters_offset(batch, num_q_heads, head_dim, num_splits) +
-           (size_t)batch * head_groups(num_q_heads) * sizeof(int32_t);
+    // last region: the warp-MMA kernel's tickets or the tcgen05 kernel's merge descriptors
+    const size_t tickets = (size_t)batch * head_groups(num_q_heads) * sizeof(int32_t);
+    const size_t descs = (size_t)2 * kTcMaxCtas * 8 * sizeof(int32_t);
+    return counters_offset(batch, num_q_heads, head_dim, num_splits) + (tickets > descs ? tickets : descs);
 }
 
 int mqa_decode_auto_splits(const mqa_batch *batch, int32_t window, int32_t num_q_heads, int32_t head_dim,
@@ -389,9 +394,12 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
         a.o_partial = static_cast<float *>(workspace);
         a.lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                           lse_offset(batch->batch, num_q_heads, D, plan.num_splits));
-        if (tc || plan.num_splits <= kMaxFusedSplits)
-            a.counters = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
-                                                     counters_offset(batch->batch, num_q_heads, D, plan.num_splits));
+        int32_t *last = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                                    counters_offset(batch->batch, num_q_heads, D, plan.num_splits));
+        if (tc)
+            a.merge_desc = last;  // rewritten by every call: no zeroing
+        else if (plan.num_splits <= kMaxFusedSplits)
+            a.counters = last;
     }
     if (tc) {
         const long long pairs = (long long)batch->batch * head_groups(num_q_heads);

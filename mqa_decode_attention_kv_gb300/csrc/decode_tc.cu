@@ -10,9 +10,11 @@
 // a (b, g) pair that lies inside one share is the whole pair: its output is
 // written directly (bf16).  A pair cut by share boundaries leaves an fp32
 // partial (O, lse) per piece in slot 0 (the share's first piece) or 1 (its
-// last) of the CTA that computed it; the last piece to finish (an atomic
-// ticket per pair) merges them once its CTA has run out of blocks.  In the
-// whole-sequence mode CTA c computes pair c alone and needs no workspace.
+// last) of the CTA that computed it, and the CTA holding its last piece
+// writes a merge descriptor; a second kernel merges every cut pair, a CTA per
+// (pair, 8 heads).  Each CTA rewrites both of its descriptor slots on every
+// call, so the workspace needs no zeroing.  In the whole-sequence mode CTA c
+// computes pair c alone and needs no workspace.
 //
 // Roles (9 warps, one CTA per SM):
 //   warps 0-3  converters.  Thread t owns token row t of every block.  Waits
@@ -68,7 +70,7 @@ struct TcCfg {
     static constexpr int OFF_MREF = OFF_RED + 160 * 4;          // softmax group: reference maxima [32], factors [32]
     static constexpr int OFF_CRED = OFF_MREF + 64 * 4;          // converter group: [4] fp32, gh[4]
     static constexpr int OFF_OK = OFF_CRED + 16 * 4;            // [RING][8] box arrived
-    static constexpr int OFF_MISC = OFF_OK + RING * BOXES * 4;  // tmem base, abort flag, start, merges
+    static constexpr int OFF_MISC = OFF_OK + RING * BOXES * 4;  // tmem base, abort flag, start position
     static constexpr int OFF_MBAR = OFF_MISC + 256;
     static constexpr int NBAR = 4 * RING + 5 * DEPTH + 4;  // tiles, 5 x DEPTH hand-offs, O free [2], Q full / free
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
@@ -395,8 +397,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 4);
     int *start_pos = reinterpret_cast<int *>(base + C::OFF_MISC + 16);          // b, g, blk, n
     long long *share = reinterpret_cast<long long *>(base + C::OFF_MISC + 32);  // first entry, N, CTAs
-    int *merges = reinterpret_cast<int *>(base + C::OFF_MISC + 64);             // count, [2][5]
-    static_assert(32 + 3 * 8 <= 64 && 64 + 11 * 4 <= 256, "misc layout");
+    static_assert(32 + 3 * 8 <= 64, "misc layout");
     uint64_t *tfull = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][2] tile codes landed (TMA)
     uint64_t *tfree = tfull + 2 * RING;         // [RING] stage free: O^T of its block done (tensor core)
     uint64_t *kready = tfree + 2 * RING;        // [DEPTH] K in tensor memory, scales, Q (4 converter warps)
@@ -564,6 +565,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         }
     }
     const int n = start_pos[3];
+    if (balanced && tid == 0) {
+        // both merge slots of this CTA start empty on every call (set below if needed)
+        a.merge_desc[(2 * cta) * 8] = -1;
+        a.merge_desc[(2 * cta + 1) * 8] = -1;
+    }
     if (n <= 0)
         return;  // uniform: nothing to compute
     const long long list_first = share[0], list_n = share[1];
@@ -592,7 +598,6 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         mbar_init(qfull, 1);
         mbar_init(qfree, 4);
         *abort_flag = 0;
-        merges[0] = 0;
         fence_mbar_init();
     }
     if (warp == 8)
@@ -1084,24 +1089,16 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     for (int j = 0; j < NH; ++j)
                         dst[(size_t)j * D] = __uint_as_float(ov[j]) * ofac_s[j];
                 }
-                if (!whole_pair) {
-                    // ticket: the last piece of the pair to finish merges it
-                    __threadfence();
-                    named_bar(BAR_SM, 128);
-                    if (tok == 0) {
-                        const long long g0 = list_first + i - cur.blk, g1 = g0 + cur.nblk - 1;
-                        const int c_lo = cta_of(g0, list_n, Ge), c_hi = cta_of(g1, list_n, Ge);
-                        const int ticket = atomicAdd(a.counters + (size_t)cur.b * groups + cur.g, 1);
-                        if (ticket == c_hi - c_lo) {
-                            const int k = merges[0]++;
-                            int *m = merges + 1 + 5 * k;
-                            m[0] = cur.b;
-                            m[1] = cur.g;
-                            m[2] = c_lo;
-                            m[3] = c_hi;
-                            m[4] = (list_n * c_lo / Ge == g0) ? 0 : 1;  // slot of the pair in CTA c_lo
-                        }
-                    }
+                if (!whole_pair && cur.blk == cur.nblk - 1 && tok == 0) {
+                    // the pair's last piece: describe the pair for the merge kernel
+                    const long long g0 = list_first + i - cur.blk, g1 = g0 + cur.nblk - 1;
+                    const int c_lo = cta_of(g0, list_n, Ge), c_hi = cta_of(g1, list_n, Ge);
+                    int *m = a.merge_desc + (2 * cta + slot) * 8;
+                    m[0] = cur.b;
+                    m[1] = cur.g;
+                    m[2] = c_lo;
+                    m[3] = c_hi;
+                    m[4] = (list_n * c_lo / Ge == g0) ? 0 : 1;  // slot of the pair in CTA c_lo
                 }
                 named_bar(BAR_SM, 128);  // red is reused by the next piece
             }
@@ -1119,80 +1116,57 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    // ---- deferred merges of the pairs whose last piece finished here: thread t of
-    // warps 0-7 merges head t / 8, d = 16 (t % 8) .. +15.  The 8 lanes of a head
-    // load its pieces' lse values together; the weights go through shared memory
-    // (the idle ring); the partial rows stream with 16 loads in flight per thread.
-    if (!aborted && warp < 8) {
-        const int nm = merges[0];
-        if (nm > 0)
-            __threadfence();
-        float *wts = reinterpret_cast<float *>(base + C::OFF_RING);  // [32 heads][np]
-        const int jh = tid >> 3, sub = tid & 7, d0 = sub * 16;
-        for (int k = 0; k < nm; ++k) {
-            const int *m = merges + 1 + 5 * k;
-            const int mb = m[0], mgp = m[1], c_lo = m[2], c_hi = m[3], slot_lo = m[4];
-            const int np = c_hi - c_lo + 1;  // <= CTAs of the grid: [32][np] floats fit the ring
-            const int h = mgp * NH + jh;
-            float M = -INFINITY;
-            for (int p = sub; p < np; p += 8)
-                M = fmaxf(M, __ldcg(a.lse + merge_row(c_lo, p, slot_lo, jh)));
+}
+
+// Merge the pieces of one cut (sequence, head group) pair, 8 heads per CTA:
+// warp k takes head 8 blockIdx.y + k, lane d = 4 lane .. 4 lane + 3.  The
+// flash-decoding combine: M = max lse, w = exp(lse - M), out = sum w o / sum w.
+__global__ void __launch_bounds__(256) decode_tc_merge_kernel(const __grid_constant__ DecodeArgs a)
+{
+    constexpr int NH = TcCfg::NH, D = TcCfg::D;
+    const int *m = a.merge_desc + blockIdx.x * 8;
+    const int b = __ldg(m);
+    if (b < 0)
+        return;
+    const int g = __ldg(m + 1), c_lo = __ldg(m + 2), c_hi = __ldg(m + 3), slot_lo = __ldg(m + 4);
+    const int np = c_hi - c_lo + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int jh = blockIdx.y * 8 + warp, h = g * NH + jh;
+    if (h >= a.num_q_heads)
+        return;
+    float M = -INFINITY;
+    for (int p = lane; p < np; p += 32)
+        M = fmaxf(M, __ldg(a.lse + merge_row(c_lo, p, slot_lo, jh)));
 #pragma unroll
-            for (int off = 1; off < 8; off <<= 1)
-                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            float den = 0.f;
-            for (int p = sub; p < np; p += 8) {
-                const float ls = __ldcg(a.lse + merge_row(c_lo, p, slot_lo, jh));
-                const float wv = (ls == -INFINITY || M == -INFINITY) ? 0.f : __expf(ls - M);
-                wts[jh * np + p] = wv;
-                den += wv;
-            }
+    for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < np; p0 += 8) {
+        float wgt[8];
+        float4 x[8];
 #pragma unroll
-            for (int off = 1; off < 8; off <<= 1)
-                den += __shfl_xor_sync(0xffffffffu, den, off);
-            __syncwarp();
-            float4 acc[4];
+        for (int u = 0; u < 8; ++u) {
+            const int p = min(p0 + u, np - 1);
+            const size_t row = merge_row(c_lo, p, slot_lo, jh);
+            const float ls = __ldg(a.lse + row);
+            wgt[u] = (p0 + u >= np || ls == -INFINITY || M == -INFINITY) ? 0.f : __expf(ls - M);
+            x[u] = __ldg(reinterpret_cast<const float4 *>(a.o_partial + row * D) + lane);
+        }
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p0 = 0; p0 < np; p0 += 4) {
-                float4 x[4][4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int p = min(p0 + u, np - 1);
-                    const float4 *src =
-                        reinterpret_cast<const float4 *>(a.o_partial + merge_row(c_lo, p, slot_lo, jh) * D + d0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        x[u][q] = __ldcg(src + q);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float wv = p0 + u < np ? wts[jh * np + p0 + u] : 0.f;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[q].x += wv * x[u][q].x;
-                        acc[q].y += wv * x[u][q].y;
-                        acc[q].z += wv * x[u][q].z;
-                        acc[q].w += wv * x[u][q].w;
-                    }
-                }
-            }
-            if (h < a.num_q_heads) {
-                const float f = den > 0.f ? 1.f / den : 0.f;
-                uint32_t pk[8];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    pk[2 * q] = pack_bf16x2(acc[q].x * f, acc[q].y * f);
-                    pk[2 * q + 1] = pack_bf16x2(acc[q].z * f, acc[q].w * f);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)mb * a.num_q_heads + h) * D + d0);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
-            __syncwarp();  // wts reused by the next merge
+        for (int u = 0; u < 8; ++u) {
+            den += wgt[u];
+            acc.x += wgt[u] * x[u].x;
+            acc.y += wgt[u] * x[u].y;
+            acc.z += wgt[u] * x[u].z;
+            acc.w += wgt[u] * x[u].w;
         }
     }
+    const float f = den > 0.f ? 1.f / den : 0.f;
+    uint2 o;
+    o.x = pack_bf16x2(acc.x * f, acc.y * f);
+    o.y = pack_bf16x2(acc.z * f, acc.w * f);
+    *reinterpret_cast<uint2 *>(a.out + ((size_t)b * a.num_q_heads + h) * D + 4 * lane) = o;
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s)
@@ -1206,6 +1180,10 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s)
         attr_set.store(1, std::memory_order_release);
     }
     decode_tc_kernel<<<a.persist_ctas, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !a.persistent)
+        return e;
+    decode_tc_merge_kernel<<<dim3(2 * a.persist_ctas, TcCfg::NH / 8), 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

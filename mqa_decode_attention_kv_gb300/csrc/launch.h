@@ -38,11 +38,13 @@ struct DecodeArgs {
     // lse rows [2 * persist_ctas][32], tickets in counters); 0 = one CTA per
     // (sequence, head group), persist_ctas = batch * head groups
     int32_t persistent, persist_ctas;
+    int32_t *merge_desc;               // [2 * persist_ctas][8]: cut pairs to merge (written by every call)
 };
 cudaError_t launch_decode(const DecodeArgs &a, int head_dim, cudaStream_t s);
 // head_dim 128 with 32 or 64 query heads runs on the tcgen05 kernel; the rest on the warp-MMA kernel
 inline bool decode_uses_tc(int head_dim, int num_q_heads) { return head_dim == 128 && num_q_heads >= 32; }
 cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s);
+constexpr int kTcMaxCtas = 1024;   // balanced tcgen05 decode: at most this many CTAs (merge slots: 2 each)
 int decode_tc_ctas_per_sm();
 int decode_ctas_per_sm(int head_dim, int num_q_heads);
 constexpr int kMaxFusedSplits = 16;  // the decode kernel merges up to this many splits itself

@@ -52,7 +52,8 @@ def test_workspace_size_formula(L):
     part = 8 * 10 * 32 * 128 * 4           # fp32 partial outputs
     lse = 8 * 10 * 32 * 4                  # fp32 log-sum-exps
     tickets = 8 * 1 * 4                    # one int32 per (sequence, group of 32 heads)
-    assert n == r256(r256(part) + lse) + tickets
+    descs = 2 * 1024 * 8 * 4               # or the tcgen05 kernel's merge descriptors, if larger
+    assert n == r256(r256(part) + lse) + max(tickets, descs)
 
 
 def cache(num_blocks=16, page=16, d=64, **kw):
