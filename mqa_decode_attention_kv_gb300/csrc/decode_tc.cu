@@ -57,7 +57,7 @@ struct TcCfg {
     static constexpr int BOXES = BT / kChunkTokens;  // 8 TMA boxes of 16 tokens
     static constexpr int RING = 5;                   // ring stages (codes in flight, then fp16 V)
     static constexpr int DEPTH = 3;                  // blocks in flight between roles (S, K, P, scales)
-    static constexpr int THREADS = 320;              // 4 converter + 4 softmax warps, MMA warp, TMA warp
+    static constexpr int THREADS = 448;              // 4 converter + 8 softmax warps, MMA warp, TMA warp
     static constexpr int CODES = BT * D;             // int8 bytes of K (or V) of a block
     static constexpr int STAGE = 2 * CODES;          // K codes, V codes; then fp16 V in place
     // shared memory (offsets from a 1024-aligned base)
@@ -150,6 +150,27 @@ __device__ __forceinline__ uint32_t ph2(int i) { return (uint32_t)(i >> 1) & 1u;
 // Buffer and phase parity of block i on a DEPTH-buffer hand-off (i >= 0).
 __device__ __forceinline__ int bufd(int i) { return i % TcCfg::DEPTH; }
 __device__ __forceinline__ uint32_t phd(int i) { return (uint32_t)(i / TcCfg::DEPTH) & 1u; }
+
+// Reduce 16 per-head values over the 32 lanes of a warp with 16 shuffles (the
+// butterfly below over each half-warp, then one exchange between the halves):
+// lane L returns the reduction of head L % 16.  v is consumed.
+template <bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lane)
+{
+#pragma unroll
+    for (int s = 8; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int k = 0; k < s; ++k) {
+            const float send = up ? v[k] : v[k + s];
+            const float keep = up ? v[k + s] : v[k];
+            const float got = __shfl_xor_sync(0xffffffffu, send, s);
+            v[k] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
+    return MAX ? fmaxf(v[0], other) : v[0] + other;
+}
 
 // Reduce 32 per-head values over the 32 lanes of a warp with 31 shuffles (a
 // butterfly that halves the values each lane keeps at every step): lane L
@@ -402,10 +423,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     uint64_t *tfree = tfull + 2 * RING;         // [RING] stage free: O^T of its block done (tensor core)
     uint64_t *kready = tfree + 2 * RING;        // [DEPTH] K in tensor memory, scales, Q (4 converter warps)
     uint64_t *vready = kready + C::DEPTH;       // [DEPTH] fp16 V in shared memory     (4 converter warps)
-    uint64_t *pready = vready + C::DEPTH;       // [DEPTH] P' written, S read          (4 softmax warps)
+    uint64_t *pready = vready + C::DEPTH;       // [DEPTH] P' written, S read          (8 softmax warps)
     uint64_t *sfull = pready + C::DEPTH;        // [DEPTH] S^T = K Q^T done            (tensor core)
     uint64_t *odone = sfull + C::DEPTH;         // [DEPTH] O^T += V^T P' done          (tensor core)
-    uint64_t *ofree = odone + C::DEPTH;         // [2] a piece's O read by its epilogue (4 softmax warps)
+    uint64_t *ofree = odone + C::DEPTH;         // [2] a piece's O read by its epilogue (8 softmax warps)
     uint64_t *qfull = ofree + 2;                // raw Q of the next piece landed      (bulk copy)
     uint64_t *qfree = qfull + 1;                // raw Q read by every converter warp  (4 converter warps)
 
@@ -589,18 +610,18 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         for (int s = 0; s < C::DEPTH; ++s) {
             mbar_init(kready + s, 4);
             mbar_init(vready + s, 4);
-            mbar_init(pready + s, 4);
+            mbar_init(pready + s, 8);
             mbar_init(sfull + s, 1);
             mbar_init(odone + s, 1);
         }
         for (int s = 0; s < 2; ++s)
-            mbar_init(ofree + s, 4);
+            mbar_init(ofree + s, 8);
         mbar_init(qfull, 1);
         mbar_init(qfree, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 8)
+    if (warp == 12)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -722,17 +743,13 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     ++q_issued;
                 }
             }
-            // ---- this token's K and V codes, every chunk loaded before any store
-            uint4 kc[D / 16], vc[D / 16];
+            // ---- this token's K codes (all chunks loaded before the conversion)
+            uint4 kc[D / 16];
             {
                 const uint8_t *krow = st + tok * D;
-                const uint8_t *vrow = st + C::CODES + tok * D;
 #pragma unroll
-                for (int j = 0; j < D / 16; ++j) {
-                    const uint32_t so = (uint32_t)(j ^ (tok & 7)) << 4;
-                    kc[j] = *reinterpret_cast<const uint4 *>(krow + so);
-                    vc[j] = *reinterpret_cast<const uint4 *>(vrow + so);
-                }
+                for (int j = 0; j < D / 16; ++j)
+                    kc[j] = *reinterpret_cast<const uint4 *>(krow + ((uint32_t)(j ^ (tok & 7)) << 4));
             }
             {
                 const int pos = (cur.t_first + 2 * cur.blk) * kTileTokens + tok;
@@ -766,6 +783,13 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             // rows are in registers once the warp passes the barrier): the MN-major A operand
             // of O^T += V^T P', token group g = lane / 8 of the warp at (g < 2 ? K half :
             // V half) + 4096 warp + 2048 (g % 2), row lane % 8 of its 16 core matrices.
+            uint4 vc[D / 16];
+            {
+                const uint8_t *vrow = st + C::CODES + tok * D;
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j)
+                    vc[j] = *reinterpret_cast<const uint4 *>(vrow + ((uint32_t)(j ^ (tok & 7)) << 4));
+            }
             __syncwarp();
             {
                 const int g = lane >> 3;
@@ -807,7 +831,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         }
         if (*abort_flag && lane == 0 && warp == 0 && q_issued > piece + 1)
             mbar_wait_bounded(qfull, (uint32_t)(q_issued - 1) & 1u);  // the Q copy still in flight (bounded)
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ================================================================ TMA producer
         // ring stage j % RING takes block j once O^T of block j - RING has read its V;
         // lane 4t + c fetches the block id of box c of tile t a block ahead
@@ -840,7 +864,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 for (int t = 0; t < 2; ++t)
                     mbar_wait_bounded(tfull + 2 * (jj % RING) + t, (uint32_t)(jj / RING) & 1u);
         }
-    } else if (warp == 8) {
+    } else if (warp == 12) {
         // ================================================================ MMA issuer
         if (lane == 0) {
             // descriptors of the shared-memory operands at their buffers' starts
@@ -886,10 +910,13 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         }
     } else {
         // ================================================================ softmax
-        const int sw = warp - 4, tok = tid - 128;
+        // thread (token tok, head half hh): warps 4-7 take heads 0-15 of their tokens,
+        // warps 8-11 heads 16-31; tensor-memory lanes by warp % 4
+        constexpr int NHH = NH / 2;
+        const int sw = warp - 4, hh = sw >> 2, tok = 32 * (warp & 3) + lane;
         // per head: this token's sum of p.  The reference maxima (log2 domain),
         // the same in every softmax thread, live in mref (shared memory).
-        float l_acc[NH];
+        float l_acc[NHH];
         int E_run = -100;         // running power-of-two bound of the V scales
         float gh = 0.f;           // log2-domain factor of the raw scores of the piece
         int piece = -1, piece_first_i = 0;
@@ -905,7 +932,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 piece_from_start = cur.blk == 0;
                 E_run = -100;
 #pragma unroll
-                for (int j = 0; j < NH; ++j)
+                for (int j = 0; j < NHH; ++j)
                     l_acc[j] = 0.f;
             }
             bool ok = wait_phase(kready + buf, phd(i), abort_flag);
@@ -915,11 +942,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             const bool valid = scb[2 * BT + tok] != 0.f;
             if (first)
                 gh = cred[4 + (piece & 3)];  // 4 slots: the converters run up to DEPTH blocks ahead
-            float mr[NH];  // the reference maxima, kept in registers while they hold
+            float mr[NHH];  // the reference maxima of this thread's heads, in registers while they hold
             if (!first) {
 #pragma unroll
-                for (int q = 0; q < NH / 4; ++q) {
-                    const float4 m4 = reinterpret_cast<const float4 *>(mref)[q];
+                for (int q = 0; q < NHH / 4; ++q) {
+                    const float4 m4 = reinterpret_cast<const float4 *>(mref + NHH * hh)[q];
                     mr[4 * q] = m4.x;
                     mr[4 * q + 1] = m4.y;
                     mr[4 * q + 2] = m4.z;
@@ -928,96 +955,90 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             }
             ok = ok && wait_phase(sfull + buf, phd(i), abort_flag);
             tc_fence_after();
-            uint32_t sr[NH];
-            {
-                uint32_t s0[16], s1[16];
-                tmem_ld16(tmem + lane_base + C::S_COL + (uint32_t)buf * NH, s0);
-                tmem_ld16(tmem + lane_base + C::S_COL + (uint32_t)buf * NH + 16, s1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    sr[j] = s0[j];
-                    sr[16 + j] = s1[j];
-                }
-            }
+            uint32_t sr[NHH];
+            tmem_ld16(tmem + lane_base + C::S_COL + (uint32_t)buf * NH + NHH * hh, sr);
+            tmem_wait_ld();
             const float kg = ksv * gh;  // raw score -> log2 domain
             // a piece's first block always moves the references (they start at -inf)
             bool need = valid && (first || !(vsv <= exp2i(E_run)));
             if (!first) {
 #pragma unroll
-                for (int j = 0; j < NH; ++j)
+                for (int j = 0; j < NHH; ++j)
                     need |= valid && !(fmaf(__uint_as_float(sr[j]), kg, -mr[j]) <= 8.f);
             }
-            if (named_bar_or(BAR_SM, 128, need || !ok)) {
-                if (named_bar_or(BAR_SM, 128, !ok))
+            if (named_bar_or(BAR_SM, 256, need || !ok)) {
+                if (named_bar_or(BAR_SM, 256, !ok))
                     break;  // abort (every softmax thread leaves here together)
                 // rare: move the references to the block maxima (and the V-scale bound)
                 {
-                    float mv[NH];
+                    float mv[NHH];
 #pragma unroll
-                    for (int j = 0; j < NH; ++j)
+                    for (int j = 0; j < NHH; ++j)
                         mv[j] = valid ? __uint_as_float(sr[j]) * kg : -INFINITY;
-                    red[sw * NH + lane] = warp_transpose_reduce<true>(mv, lane);  // head lane's warp maximum
+                    const float wm = warp_transpose_reduce16<true>(mv, lane);  // head lane % 16's warp max
+                    if (lane < NHH)
+                        red[sw * NHH + lane] = wm;
                 }
                 float vm = valid ? vsv : 0.f;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1)
                     vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
                 if (lane == 0)
-                    red[4 * NH + sw] = vm;
-                named_bar(BAR_SM, 128);
-                const float vmax = fmaxf(fmaxf(red[4 * NH], red[4 * NH + 1]), fmaxf(red[4 * NH + 2], red[4 * NH + 3]));
+                    red[8 * NHH + sw] = vm;
+                named_bar(BAR_SM, 256);
+                float vmax = red[8 * NHH];
+#pragma unroll
+                for (int k = 1; k < 8; ++k)
+                    vmax = fmaxf(vmax, red[8 * NHH + k]);
                 const int E_new = max(E_run, ceil_log2_pow(vmax));
                 const int dE = E_run - E_new;
                 const float escale = dE < -126 ? 0.f : exp2i(dE);
-                // thread tok < 32 moves head tok's reference; every thread rescales its l
-                if (tok < NH) {
-                    const float bm = fmaxf(fmaxf(red[tok], red[NH + tok]), fmaxf(red[2 * NH + tok], red[3 * NH + tok]));
-                    const float mo = first ? -INFINITY : mref[tok];
+                // warp 4 moves the references (lane = head, over the 4 warps of its half)
+                if (sw == 0) {
+                    const int h = lane, base4 = 4 * (h >> 4) * NHH + (h & 15);
+                    const float bm = fmaxf(fmaxf(red[base4], red[base4 + NHH]),
+                                           fmaxf(red[base4 + 2 * NHH], red[base4 + 3 * NHH]));
+                    const float mo = first ? -INFINITY : mref[h];
                     const float mn = fmaxf(mo, bm);
-                    const float fl = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
-                    mref[tok] = mn;
-                    ofac_s[tok] = fl;
+                    mref[h] = mn;
+                    ofac_s[h] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
                 }
-                named_bar(BAR_SM, 128);
+                named_bar(BAR_SM, 256);
 #pragma unroll
-                for (int j = 0; j < NH; ++j)
-                    l_acc[j] *= ofac_s[j];
+                for (int j = 0; j < NHH; ++j)
+                    l_acc[j] *= ofac_s[NHH * hh + j];
                 E_run = E_new;
                 if (!first) {
-                    // O of this piece, once O^T(i-1) has landed: row d = tok, 32 heads
+                    // O of this piece, once O^T(i-1) has landed: row d = tok, this thread's 16 heads
                     wait_phase(odone + bufd(i - 1), phd(i - 1), abort_flag);
                     tc_fence_after();
-                    const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH;
+                    const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH + NHH * hh;
+                    uint32_t orr[16];
+                    tmem_ld16(tmem + lane_base + o_col, orr);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int hq = 0; hq < 2; ++hq) {
-                        uint32_t orr[16];
-                        tmem_ld16(tmem + lane_base + o_col + 16 * hq, orr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            orr[j] = __float_as_uint(__uint_as_float(orr[j]) * (ofac_s[16 * hq + j] * escale));
-                        tmem_st16(tmem + lane_base + o_col + 16 * hq, orr);
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        orr[j] = __float_as_uint(__uint_as_float(orr[j]) * (ofac_s[NHH * hh + j] * escale));
+                    tmem_st16(tmem + lane_base + o_col, orr);
                     tmem_wait_st();
                 }
-                named_bar(BAR_SM, 128);  // reductions read before red is reused
+                named_bar(BAR_SM, 256);  // reductions read before red is reused
 #pragma unroll
-                for (int q = 0; q < NH / 4; ++q) {
-                    const float4 m4 = reinterpret_cast<const float4 *>(mref)[q];
+                for (int q = 0; q < NHH / 4; ++q) {
+                    const float4 m4 = reinterpret_cast<const float4 *>(mref + NHH * hh)[q];
                     mr[4 * q] = m4.x;
                     mr[4 * q + 1] = m4.y;
                     mr[4 * q + 2] = m4.z;
                     mr[4 * q + 3] = m4.w;
                 }
             }
-            // ---- P' = 2^(score - ref) * s_v * 2^(6-E) as fp16 row tok of P'[buf]
+            // ---- P' = 2^(score - ref) * s_v * 2^(6-E) as fp16: row tok, heads 16hh .. 16hh+15 of P'[buf]
             if (i >= C::DEPTH)  // P' buffer [buf] free once O^T(i-DEPTH) is done
                 wait_phase(odone + buf, phd(i - C::DEPTH), abort_flag);
             const float vf = valid ? vsv * exp2i(6 - E_run) : 0.f;
             uint8_t *pb = ph + buf * BT * NH * 2;
 #pragma unroll
-            for (int q = 0; q < NH / 8; ++q) {
+            for (int q = 0; q < NHH / 8; ++q) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -1028,7 +1049,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     l_acc[j0 + 1] += p1;
                     pk[k] = pack_half2(p0 * vf, p1 * vf);
                 }
-                *reinterpret_cast<uint4 *>(pb + core_off(tok, 8 * q, C::P_SR, C::P_SC)) =
+                *reinterpret_cast<uint4 *>(pb + core_off(tok, NHH * hh + 8 * q, C::P_SR, C::P_SC)) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
             fence_proxy_async();
@@ -1041,55 +1062,49 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 wait_phase(odone + buf, phd(i), abort_flag);  // O^T(i) landed
                 tc_fence_after();
                 {
-                    float lv[NH];
+                    float lv[NHH];
 #pragma unroll
-                    for (int j = 0; j < NH; ++j)
+                    for (int j = 0; j < NHH; ++j)
                         lv[j] = l_acc[j];
-                    red[sw * NH + lane] = warp_transpose_reduce<false>(lv, lane);  // head lane's warp sum
+                    const float ws = warp_transpose_reduce16<false>(lv, lane);  // head lane % 16's warp sum
+                    if (lane < NHH)
+                        red[sw * NHH + lane] = ws;
                 }
                 const bool whole_pair = piece_from_start && cur.blk == cur.nblk - 1;
                 const int slot = piece_first_i == 0 ? 0 : 1;
-                named_bar(BAR_SM, 128);
-                if (tok < NH) {
-                    // head tok: l, the output factor 2^(E-6) / l and (for a partial) the lse
-                    const float l = red[tok] + red[NH + tok] + red[2 * NH + tok] + red[3 * NH + tok];
-                    ofac_s[tok] = l > 0.f ? __fdividef(exp2i(E_run - 6), l) : 0.f;
-                    if (!whole_pair && cur.g * NH + tok < a.num_q_heads)
-                        a.lse[(size_t)(2 * cta + slot) * NH + tok] =
-                            l > 0.f ? (mref[tok] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                named_bar(BAR_SM, 256);
+                if (sw == 0) {
+                    // head lane: l, the output factor 2^(E-6) / l and (for a partial) the lse
+                    const int h = lane, base4 = 4 * (h >> 4) * NHH + (h & 15);
+                    const float l = red[base4] + red[base4 + NHH] + red[base4 + 2 * NHH] + red[base4 + 3 * NHH];
+                    ofac_s[h] = l > 0.f ? __fdividef(exp2i(E_run - 6), l) : 0.f;
+                    if (!whole_pair && cur.g * NH + h < a.num_q_heads)
+                        a.lse[(size_t)(2 * cta + slot) * NH + h] =
+                            l > 0.f ? (mref[h] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
                 }
-                const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH;
-                uint32_t ov[NH];
-                {
-                    uint32_t o0[16], o1[16];
-                    tmem_ld16(tmem + lane_base + o_col, o0);
-                    tmem_ld16(tmem + lane_base + o_col + 16, o1);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        ov[j] = o0[j];
-                        ov[16 + j] = o1[j];
-                    }
-                }
+                const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH + NHH * hh;
+                uint32_t ov[NHH];
+                tmem_ld16(tmem + lane_base + o_col, ov);
+                tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(ofree + (piece & 1));
-                named_bar(BAR_SM, 128);  // ofac_s ready
+                named_bar(BAR_SM, 256);  // ofac_s ready
                 const int nh = min(NH, a.num_q_heads - cur.g * NH);  // heads of this group that exist
                 if (whole_pair) {
-                    __nv_bfloat16 *dst = a.out + ((size_t)cur.b * a.num_q_heads + cur.g * NH) * D + tok;
+                    __nv_bfloat16 *dst = a.out + ((size_t)cur.b * a.num_q_heads + cur.g * NH + NHH * hh) * D + tok;
 #pragma unroll
-                    for (int j = 0; j < NH; ++j)
-                        if (j < nh)
-                            dst[(size_t)j * D] = __float2bfloat16_rn(__uint_as_float(ov[j]) * ofac_s[j]);
+                    for (int j = 0; j < NHH; ++j)
+                        if (NHH * hh + j < nh)
+                            dst[(size_t)j * D] = __float2bfloat16_rn(__uint_as_float(ov[j]) * ofac_s[NHH * hh + j]);
                 } else {
-                    float *dst = a.o_partial + (size_t)(2 * cta + slot) * NH * D + tok;
+                    float *dst = a.o_partial + ((size_t)(2 * cta + slot) * NH + NHH * hh) * D + tok;
 #pragma unroll
-                    for (int j = 0; j < NH; ++j)
-                        dst[(size_t)j * D] = __uint_as_float(ov[j]) * ofac_s[j];
+                    for (int j = 0; j < NHH; ++j)
+                        dst[(size_t)j * D] = __uint_as_float(ov[j]) * ofac_s[NHH * hh + j];
                 }
-                if (!whole_pair && cur.blk == cur.nblk - 1 && tok == 0) {
+                if (!whole_pair && cur.blk == cur.nblk - 1 && sw == 0 && lane == 0) {
                     // the pair's last piece: describe the pair for the merge kernel
                     const long long g0 = list_first + i - cur.blk, g1 = g0 + cur.nblk - 1;
                     const int c_lo = cta_of(g0, list_n, Ge), c_hi = cta_of(g1, list_n, Ge);
@@ -1100,7 +1115,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     m[3] = c_hi;
                     m[4] = (list_n * c_lo / Ge == g0) ? 0 : 1;  // slot of the pair in CTA c_lo
                 }
-                named_bar(BAR_SM, 128);  // red is reused by the next piece
+                named_bar(BAR_SM, 256);  // red and ofac_s are reused by the next piece
             }
             cursor_next(cur, a, groups);
         }
@@ -1112,7 +1127,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     const bool aborted = *abort_flag != 0;
     if (aborted && tid == 0)
         set_status(a.dev_status, MQA_DEV_TIMEOUT);
-    if (warp == 8) {
+    if (warp == 12) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
