@@ -62,8 +62,8 @@ struct TcCfg {
     static constexpr int STAGE = 2 * CODES;          // K codes, V codes; then fp16 V in place
     // shared memory (offsets from a 1024-aligned base)
     static constexpr int OFF_RING = 0;
-    static constexpr int OFF_QH = OFF_RING + RING * STAGE;      // fp16 Q [32 h][128 d], core layout
-    static constexpr int OFF_QRAW = OFF_QH + NH * D * 2;        // bf16 Q [32 h][128 d] as copied (next piece)
+    static constexpr int OFF_QH = OFF_RING + RING * STAGE;      // [2] fp16 Q [32 h][128 d], core layout (piece parity)
+    static constexpr int OFF_QRAW = OFF_QH + 2 * NH * D * 2;    // bf16 Q [32 h][128 d] as copied (next piece)
     static constexpr int OFF_PH = OFF_QRAW + NH * D * 2;        // [DEPTH] fp16 P' [128 tok][32 h], core layout
     static constexpr int OFF_SC = OFF_PH + DEPTH * BT * NH * 2;  // [DEPTH][3][128] fp32: K scale, V scale, valid
     static constexpr int OFF_RED = OFF_SC + DEPTH * 3 * BT * 4;  // softmax group: [4 warps][32] + [4] fp32
@@ -679,8 +679,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             }
             if (first) {
                 ok = ok && wait_phase(qfull, (uint32_t)(piece + 1) & 1u, abort_flag);  // this piece's raw Q
-                if (i >= 1)  // fp16 Q is single-buffered: every S^T(i-1) must be done
-                    ok = ok && wait_phase(sfull + bufd(i - 1), phd(i - 1), abort_flag);
+                if (i >= 2)  // fp16 Q buffer (piece parity) was last read by piece-2's S^T, done by S^T(i-2)
+                    ok = ok && wait_phase(sfull + bufd(i - 2), phd(i - 2), abort_flag);
             }
             if (!__all_sync(0xffffffffu, ok))
                 break;
@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         hv[u] = pack_half2(__uint_as_float(w4[u] << 16) * f, __uint_as_float(w4[u] & 0xffff0000u) * f);
-                    *reinterpret_cast<uint4 *>(qh + core_off(lane, 8 * c, C::Q_SR, C::Q_SC)) =
+                    *reinterpret_cast<uint4 *>(qh + (piece & 1) * NH * D * 2 + core_off(lane, 8 * c, C::Q_SR, C::Q_SC)) =
                         make_uint4(hv[0], hv[1], hv[2], hv[3]);
                 }
                 if (warp == 0 && lane == 0)
@@ -872,24 +872,29 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             const uint64_t vdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING), C::V_SR, C::V_SC);
             const uint64_t pdesc0 = umma_sdesc(smem_u32(ph), C::P_SR, C::P_SC);
             Cursor cur = c0;
-            int n_qk = 0, n_pv = 0, piece = -1;
+            int n_qk = 0, n_pv = 0, piece = -1, qpiece = -1;
             uint32_t first_bits = 0;  // bit (j & 31): block j starts a piece
             bool ok = true;
             for (int i = 0; i < n && ok; ++i) {
                 const int buf = bufd(i);
-                if (i == 0 || cur.blk == 0)
+                const bool first = i == 0 || cur.blk == 0;
+                if (first) {
                     first_bits |= 1u << (i & 31);
-                else
+                    ++qpiece;
+                } else {
                     first_bits &= ~(1u << (i & 31));
-                // S^T(i) = K(i) Q^T: K from tensor memory, Q from shared memory.  The
-                // S buffer [buf] was read by softmax(i-2), waited for before O^T(i-2).
+                }
+                // S^T(i) = K(i) Q^T: K from tensor memory, Q (this piece's buffer) from shared
+                // memory.  The S buffer [buf] was read by softmax(i-DEPTH), waited for before
+                // O^T(i-DEPTH) was issued.
                 if (!wait_phase(kready + buf, phd(i), abort_flag))
                     break;
                 tc_fence_after();
+                const uint64_t qd = desc_add(qdesc0, (uint32_t)(qpiece & 1) * NH * D * 2);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     umma_f16_ts(tmem + C::S_COL + (uint32_t)buf * NH, tmem + C::K_COL + (uint32_t)buf * 64 + 8 * kk,
-                                desc_add(qdesc0, kk * 2 * C::Q_SC), IDESC_QK, kk > 0);
+                                desc_add(qd, kk * 2 * C::Q_SC), IDESC_QK, kk > 0);
                 umma_commit(sfull + buf);
                 ++n_qk;
                 if (i >= 1)
