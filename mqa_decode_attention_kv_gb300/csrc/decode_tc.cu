@@ -1141,10 +1141,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
 // Merge the pieces of one cut (sequence, head group) pair, 8 heads per CTA:
 // warp k takes head 8 blockIdx.y + k, lane d = 4 lane .. 4 lane + 3.  The
 // flash-decoding combine: M = max lse, w = exp(lse - M), out = sum w o / sum w.
+// A cut pair's last piece always opens its CTA's share, so its descriptor is in
+// slot 0 of CTA blockIdx.x.
 __global__ void __launch_bounds__(256) decode_tc_merge_kernel(const __grid_constant__ DecodeArgs a)
 {
     constexpr int NH = TcCfg::NH, D = TcCfg::D;
-    const int *m = a.merge_desc + blockIdx.x * 8;
+    const int *m = a.merge_desc + (2 * blockIdx.x) * 8;
     const int b = __ldg(m);
     if (b < 0)
         return;
@@ -1203,7 +1205,7 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !a.persistent)
         return e;
-    decode_tc_merge_kernel<<<dim3(2 * a.persist_ctas, TcCfg::NH / 8), 256, 0, s>>>(a);
+    decode_tc_merge_kernel<<<dim3(a.persist_ctas, TcCfg::NH / 8), 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
