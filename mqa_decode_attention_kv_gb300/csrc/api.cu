@@ -162,6 +162,45 @@ int tc_max_ctas(int head_dim, int heads)
     return g < kTcMaxCtas ? g : kTcMaxCtas;
 }
 
+// 64-token tiles of a decode key range; defined below.
+int tiles_for(int L, int W);
+int tiles_bound(int Lmax, int W);
+
+// Whether the automatic plan of the tcgen05 kernel runs one CTA per (sequence,
+// head group) instead of balanced shares.  Cutting a pair between CTAs costs
+// far more than its blocks (the pieces' epilogues and reference moves, the
+// merge kernel): measured on GB300, a 24-layer step ran 17% faster with whole
+// pairs on its local layers (8-9 blocks a pair, 7.2 blocks a balanced share)
+// and 2.5x slower with them on its long global layers.  Whole pairs win when
+// waves x the longest pair stays within kWholeSlack blocks of the balanced
+// share.  Lengths come from the host copy when given, else from max_seq_len.
+constexpr int kWholeSlack = 6;
+
+bool tc_whole_pairs(const mqa_batch *bt, int window, int heads, int head_dim)
+{
+    const long long g = tc_max_ctas(head_dim, heads);
+    if (g <= 0 || bt->batch <= 0)
+        return false;
+    const long long groups = (heads + 31) / 32, pairs = (long long)bt->batch * groups;
+    long long nb = 0, maxb = 0;
+    if (bt->seq_lens_host != nullptr) {
+        for (int b = 0; b < bt->batch; ++b) {
+            const long long t = (tiles_for(bt->seq_lens_host[b], window) + 1) / 2;
+            nb += t;
+            maxb = t > maxb ? t : maxb;
+        }
+    } else {
+        maxb = (tiles_bound(bt->max_seq_len, window) + 1) / 2;
+        nb = maxb * bt->batch;
+    }
+    nb *= groups;
+    const long long ctas = g < nb ? g : nb;
+    if (ctas <= 0)
+        return true;
+    const long long waves = (pairs + g - 1) / g;
+    return waves * maxb * ctas <= nb + kWholeSlack * ctas;  // waves * maxb <= share + slack
+}
+
 int tc_auto_splits(int batch, int heads, int head_dim)
 {
     const long long g = tc_max_ctas(head_dim, heads);
@@ -340,7 +379,8 @@ int mqa_decode_auto_splits(const mqa_batch *batch, int32_t window, int32_t num_q
     if (decode_uses_tc(head_dim, num_q_heads)) {
         if (tc_max_ctas(head_dim, num_q_heads) <= 0)
             return MQA_ERR_CUDA;
-        return tc_auto_splits(batch->batch, num_q_heads, head_dim);
+        return tc_whole_pairs(batch, window, num_q_heads, head_dim) ? 1
+                                                                     : tc_auto_splits(batch->batch, num_q_heads, head_dim);
     }
     Plan p;
     rc = plan_decode(batch, window, num_q_heads, head_dim, 0, &p);
@@ -376,8 +416,10 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
         // count's workspace (the automatic count fits every resident CTA)
         plan.max_tiles = 0;
         plan.tiles_per_split = 0;
-        plan.num_splits = num_splits == 1 ? 1 : (num_splits == 0 ? tc_auto_splits(batch->batch, num_q_heads, D)
-                                                                  : num_splits);
+        plan.num_splits = num_splits;
+        if (num_splits == 0)
+            plan.num_splits = tc_whole_pairs(batch, window, num_q_heads, D) ? 1
+                                                                            : tc_auto_splits(batch->batch, num_q_heads, D);
         if (plan.num_splits > 1 && tc_max_ctas(D, num_q_heads) <= 0)
             return MQA_ERR_CUDA;
     } else {
