@@ -70,7 +70,8 @@ struct TcCfg {
     static constexpr int OFF_MREF = OFF_RED + 160 * 4;          // softmax group: reference maxima [32], factors [32]
     static constexpr int OFF_CRED = OFF_MREF + 64 * 4;          // converter group: [4] fp32, gh[4]
     static constexpr int OFF_OK = OFF_CRED + 16 * 4;            // [RING][8] box arrived
-    static constexpr int OFF_MISC = OFF_OK + RING * BOXES * 4;  // tmem base, abort flag, start position
+    static constexpr int OFF_SCL = OFF_OK + RING * BOXES * 4;   // [RING][2][128] fp32 K, V token scales (TMA)
+    static constexpr int OFF_MISC = OFF_SCL + RING * 2 * BT * 4;  // tmem base, abort flag, start position
     static constexpr int OFF_MBAR = OFF_MISC + 256;
     static constexpr int NBAR = 4 * RING + 5 * DEPTH + 4;  // tiles, 5 x DEPTH hand-offs, O free [2], Q full / free
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
@@ -89,6 +90,14 @@ struct TcCfg {
     static constexpr uint32_t P_SC = 128;       // next 8 heads
 };
 static_assert(TcCfg::SMEM_BYTES <= 227 * 1024, "shared memory budget");
+// 128-byte-swizzled TMA destinations and descriptor bases on 1024 B; bulk copies, vector
+// loads and stores on 16 B; mbarriers on 8 B
+static_assert(TcCfg::OFF_RING % 1024 == 0 && TcCfg::STAGE % 1024 == 0 && TcCfg::OFF_QH % 1024 == 0 &&
+                  TcCfg::OFF_PH % 1024 == 0, "1024-byte alignment");
+static_assert(TcCfg::OFF_QRAW % 16 == 0 && TcCfg::OFF_SC % 16 == 0 && TcCfg::OFF_RED % 16 == 0 &&
+                  TcCfg::OFF_MREF % 16 == 0 && TcCfg::OFF_CRED % 16 == 0 && TcCfg::OFF_OK % 16 == 0 &&
+                  TcCfg::OFF_SCL % 16 == 0 && TcCfg::OFF_MISC % 16 == 0 && TcCfg::OFF_MBAR % 8 == 0,
+              "16-byte alignment");
 static_assert(TcCfg::K_COL + TcCfg::DEPTH * 64 <= TcCfg::TMEM_COLS, "tensor memory budget");
 
 // Mbarrier wait with a suspend hint: a waiting warp sleeps until the phase
@@ -288,13 +297,15 @@ __device__ __forceinline__ int32_t fetch_tile_box_id(const DecodeArgs &a, const 
                : kNoBlock;
 }
 
-// Both tiles of the block at p into ring stage `stage`, issued by the TMA warp
-// (every lane calls; lane 4t + c holds the id of box c of tile t).  A tile
-// inside [lo, L) on one 64-token page goes as one 64-row copy per tensor, any
-// other tile as its 16-row boxes that overlap [lo, L).  One arrival per tile
-// on bars[t] with its byte count; box_ok[4t + c] records whether box c comes.
+// Both tiles of the block at p into ring stage `stage`, their token scales into
+// `scl` ([2][128] fp32: K, V), issued by the TMA warp (every lane calls; lane
+// 4t + c holds the id of box c of tile t).  A tile inside [lo, L) on one
+// 64-token page goes as one 64-row copy per tensor (and one 256-byte copy per
+// scale row), any other tile as its 16-row boxes that overlap [lo, L) (and
+// 64-byte scale copies).  One arrival per tile on bars[t] with its byte count;
+// box_ok[4t + c] records whether box c comes.
 __device__ __forceinline__ void issue_block(const DecodeArgs &a, const Cursor &p, int lane, int32_t idc,
-                                            uint8_t *stage, uint64_t *bars, uint32_t *oks)
+                                            uint8_t *stage, float *scl, uint64_t *bars, uint32_t *oks)
 {
     constexpr int D = TcCfg::D;
 #pragma unroll
@@ -311,44 +322,27 @@ __device__ __forceinline__ void issue_block(const DecodeArgs &a, const Cursor &p
             oks[4 * t + c] = row >= 0 ? 1u : 0u;
         __syncwarp();  // the flags are written before the arrival (a tile with nothing to fetch completes on it)
         if (lane == 0)
-            mbar_arrive_expect_tx(bars + t, 2u * (uint32_t)__popc(okmask) * kChunkTokens * D);
+            mbar_arrive_expect_tx(bars + t, 2u * (uint32_t)__popc(okmask) * kChunkTokens * (D + 4));
         __syncwarp();
         if (whole) {
             if (lane == 0) {
                 tma_load_2d(stage + t * kTileTokens * D, &a.k_map64, 0, row0, bars + t);
                 tma_load_2d(stage + TcCfg::CODES + t * kTileTokens * D, &a.v_map64, 0, row0, bars + t);
+                bulk_load(scl + t * kTileTokens, a.k_scale + row0, kTileTokens * 4, bars + t);
+                bulk_load(scl + TcCfg::BT + t * kTileTokens, a.v_scale + row0, kTileTokens * 4, bars + t);
             }
         } else if (row >= 0) {
             const int box = 4 * t + c;
             tma_load_2d(stage + box * kChunkTokens * D, &a.k_map, 0, row, bars + t);
             tma_load_2d(stage + TcCfg::CODES + box * kChunkTokens * D, &a.v_map, 0, row, bars + t);
+            bulk_load(scl + box * kChunkTokens, a.k_scale + row, kChunkTokens * 4, bars + t);
+            bulk_load(scl + TcCfg::BT + box * kChunkTokens, a.v_scale + row, kChunkTokens * 4, bars + t);
         }
     }
 }
 
-// This thread's token scales for the block at p (token tok: box tok >> 4), 0
-// when its box is not fetched.
-__device__ __forceinline__ void load_token_scales(const DecodeArgs &a, const Cursor &p, int tok, int32_t id,
-                                                  float &ks, float &vs)
-{
-    const int row = box_row(a, id, p.t_first + 2 * p.blk + (tok >> 6), (tok >> 4) & 3);
-    ks = row >= 0 ? __ldg(a.k_scale + row + (tok & 15)) : 0.f;
-    vs = row >= 0 ? __ldg(a.v_scale + row + (tok & 15)) : 0.f;
-}
-
 // Shared-memory descriptor plus a byte offset (the address field counts 16 B).
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
-
-// Q row of head `lane` of the group at p (128 bf16 = 16 uint4) into registers;
-// the four uint4 of the d range warp w converts (32w .. 32w+31) come first.
-__device__ __forceinline__ void load_q_row(const DecodeArgs &a, const Cursor &p, int w, int lane, uint4 (&qv)[16])
-{
-    const int h = p.g * TcCfg::NH + lane;
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)p.b * a.num_q_heads + h) * TcCfg::D);
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-        qv[k] = h < a.num_q_heads ? __ldg(src + ((k + 4 * w) & 15)) : make_uint4(0, 0, 0, 0);
-}
 
 // O^T += V^T(j) P'(j) for block j into the O buffer of its piece (MMA thread).
 // Returns false when a wait gave up.
@@ -414,6 +408,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     float *ofac_s = mref + NH;                                     // [32] per-head O rescale factors
     float *cred = reinterpret_cast<float *>(base + C::OFF_CRED);
     uint32_t *box_ok = reinterpret_cast<uint32_t *>(base + C::OFF_OK);
+    float *scl = reinterpret_cast<float *>(base + C::OFF_SCL);  // [RING][2][128] token scales, with the codes
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 4);
     int *start_pos = reinterpret_cast<int *>(base + C::OFF_MISC + 16);          // b, g, blk, n
@@ -634,27 +629,9 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         // ================================================================ converters
         const int tok = tid;  // token row of every block = tensor-memory lane
         const int my_tile = warp >> 1;            // warps 0, 1 read tile 0 of a block; warps 2, 3 tile 1
-        Cursor cur = c0, pre = c0;
-        int n_issued = 0, q_issued = 0;
-        float ksr[RING], vsr[RING];  // scales of this thread's token in blocks i .. i+RING-1
+        Cursor cur = c0;
+        int q_issued = 0;
         {
-            // scales of this thread's token in the first RING blocks: ids first, then the loads
-            int32_t ids[RING];
-            Cursor p = c0;
-#pragma unroll
-            for (int j = 0; j < RING; ++j) {
-                ids[j] = j < n ? fetch_tile_box_id(a, p, tok >> 6, (tok >> 4) & 3) : kNoBlock;
-                cursor_next(p, a, groups);
-            }
-#pragma unroll
-            for (int j = 0; j < RING; ++j) {
-                ksr[j] = vsr[j] = 0.f;
-                if (j < n) {
-                    load_token_scales(a, pre, tok, ids[j], ksr[j], vsr[j]);
-                    cursor_next(pre, a, groups);
-                    ++n_issued;
-                }
-            }
             // the first piece's Q (bf16, 32 heads x 256 B, contiguous)
             if (warp == 0 && lane == 0) {
                 mbar_arrive_expect_tx(qfull, NH * D * 2);
@@ -662,15 +639,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             }
             q_issued = 1;
         }
-        int32_t idn = kNoBlock;  // this token's box id in block n_issued, fetched an iteration ahead
         int piece = -1;
         int i = 0;
         for (; i < n; ++i) {
             const int r = i % RING, buf = bufd(i);
             uint8_t *st = base + C::OFF_RING + r * C::STAGE;
             const bool first = (i == 0) || cur.blk == 0;
-            if (n_issued < n)  // used by this iteration's scale loads
-                idn = fetch_tile_box_id(a, pre, tok >> 6, (tok >> 4) & 3);
             bool ok = wait_phase(tfull + 2 * r + my_tile, (uint32_t)(i / RING) & 1u, abort_flag);
             if (i >= C::DEPTH) {
                 // K buffer [buf] free once S^T(i-DEPTH) is done; scale slot [buf] once softmax(i-DEPTH) is
@@ -753,10 +727,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             }
             {
                 const int pos = (cur.t_first + 2 * cur.blk) * kTileTokens + tok;
-                const bool valid = box_ok[r * C::BOXES + (tok >> 4)] != 0 && pos >= cur.lo && pos < cur.L;
+                const bool fetched = box_ok[r * C::BOXES + (tok >> 4)] != 0;
+                const bool valid = fetched && pos >= cur.lo && pos < cur.L;
+                const float *sr = scl + r * 2 * BT;  // landed with the codes
                 float *scb = sc + buf * 3 * BT;
-                scb[tok] = ksr[0];
-                scb[BT + tok] = vsr[0];
+                scb[tok] = fetched ? sr[tok] : 0.f;
+                scb[BT + tok] = fetched ? sr[BT + tok] : 0.f;
                 scb[2 * BT + tok] = valid ? 1.f : 0.f;
             }
             // ---- K: 128 codes -> fp16 pairs in tensor memory (lane tok, 64 columns)
@@ -815,18 +791,6 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(vready + buf);
-            // ---- scales of this thread's token in block n_issued (its codes come from the TMA warp)
-#pragma unroll
-            for (int j = 0; j + 1 < RING; ++j) {
-                ksr[j] = ksr[j + 1];
-                vsr[j] = vsr[j + 1];
-            }
-            ksr[RING - 1] = vsr[RING - 1] = 0.f;
-            if (n_issued < n) {
-                load_token_scales(a, pre, tok, idn, ksr[RING - 1], vsr[RING - 1]);
-                cursor_next(pre, a, groups);
-                ++n_issued;
-            }
             cursor_next(cur, a, groups);
         }
         if (*abort_flag && lane == 0 && warp == 0 && q_issued > piece + 1)
@@ -853,7 +817,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             Cursor nx = pre;
             cursor_next(nx, a, groups);
             const int32_t id_next = (lane < 8 && j + 1 < n) ? fetch_tile_box_id(a, nx, lane >> 2, lane & 3) : kNoBlock;
-            issue_block(a, pre, lane, idc, base + C::OFF_RING + r * C::STAGE, tfull + 2 * r, box_ok + r * C::BOXES);
+            issue_block(a, pre, lane, idc, base + C::OFF_RING + r * C::STAGE, scl + r * 2 * BT, tfull + 2 * r,
+                        box_ok + r * C::BOXES);
             idc = id_next;
             pre = nx;
         }
