@@ -71,7 +71,9 @@ struct TcCfg {
     static constexpr int OFF_CRED = OFF_MREF + 64 * 4;          // converter group: [4] fp32, gh[4]
     static constexpr int OFF_OK = OFF_CRED + 16 * 4;            // [RING][8] box arrived
     static constexpr int OFF_SCL = OFF_OK + RING * BOXES * 4;   // [RING][2][128] fp32 K, V token scales (TMA)
-    static constexpr int OFF_MISC = OFF_SCL + RING * 2 * BT * 4;  // tmem base, abort flag, start position
+    static constexpr int OFF_QB = OFF_SCL + RING * 2 * BT * 4;  // [4 pieces][4 warps][32] fp32 partial sums of Q
+    static constexpr int OFF_BS = OFF_QB + 4 * 4 * NH * 4;      // [32] fp32 K bias of the piece's scores
+    static constexpr int OFF_MISC = OFF_BS + NH * 4;            // tmem base, abort flag, start position
     static constexpr int OFF_MBAR = OFF_MISC + 256;
     static constexpr int NBAR = 4 * RING + 5 * DEPTH + 4;  // tiles, 5 x DEPTH hand-offs, O free [2], Q full / free
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
@@ -96,7 +98,8 @@ static_assert(TcCfg::OFF_RING % 1024 == 0 && TcCfg::STAGE % 1024 == 0 && TcCfg::
                   TcCfg::OFF_PH % 1024 == 0, "1024-byte alignment");
 static_assert(TcCfg::OFF_QRAW % 16 == 0 && TcCfg::OFF_SC % 16 == 0 && TcCfg::OFF_RED % 16 == 0 &&
                   TcCfg::OFF_MREF % 16 == 0 && TcCfg::OFF_CRED % 16 == 0 && TcCfg::OFF_OK % 16 == 0 &&
-                  TcCfg::OFF_SCL % 16 == 0 && TcCfg::OFF_MISC % 16 == 0 && TcCfg::OFF_MBAR % 8 == 0,
+                  TcCfg::OFF_SCL % 16 == 0 && TcCfg::OFF_QB % 16 == 0 && TcCfg::OFF_BS % 16 == 0 &&
+                  TcCfg::OFF_MISC % 16 == 0 && TcCfg::OFF_MBAR % 8 == 0,
               "16-byte alignment");
 static_assert(TcCfg::K_COL + TcCfg::DEPTH * 64 <= TcCfg::TMEM_COLS, "tensor memory budget");
 
@@ -341,6 +344,18 @@ __device__ __forceinline__ void issue_block(const DecodeArgs &a, const Cursor &p
     }
 }
 
+// Four codes (byte i = code c_i) -> lo = {c0, c1} + kBias, hi = {c2, c3} + kBias as f16x2,
+// exact: the exponent-bias conversion (0x64xx = 1024 + byte, on the codes offset by 128)
+// without its final subtraction.  K enters S^T = K Q^T this way; the bias adds
+// kBias * sum_d Q[h][d] to every score of head h, which the softmax warps take off in fp32.
+constexpr float kBias = 1152.f;
+__device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t t = w ^ 0x80808080u;
+    lo = __byte_perm(t, 0x64646464u, 0x5140);
+    hi = __byte_perm(t, 0x64646464u, 0x7362);
+}
+
 // Shared-memory descriptor plus a byte offset (the address field counts 16 B).
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
@@ -409,6 +424,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     float *cred = reinterpret_cast<float *>(base + C::OFF_CRED);
     uint32_t *box_ok = reinterpret_cast<uint32_t *>(base + C::OFF_OK);
     float *scl = reinterpret_cast<float *>(base + C::OFF_SCL);  // [RING][2][128] token scales, with the codes
+    float *qpart = reinterpret_cast<float *>(base + C::OFF_QB);  // [4][4][32] per-warp sums of the fp16 Q
+    float *bsum = reinterpret_cast<float *>(base + C::OFF_BS);   // [32] kBias * sum_d Q of the piece
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 4);
     int *start_pos = reinterpret_cast<int *>(base + C::OFF_MISC + 16);          // b, g, blk, n
@@ -685,6 +702,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     e = min(120, max(-120, 14 - x));
                 }
                 const float f = exp2i(e);
+                float qsum = 0.f;  // this warp's d range of head `lane`, as the tensor core sees it
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const int c = 4 * warp + ((t + lane) & 3);  // 8-d chunk: d = 8c .. 8c+7
@@ -692,11 +710,16 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
                     uint32_t hv[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < 4; ++u) {
                         hv[u] = pack_half2(__uint_as_float(w4[u] << 16) * f, __uint_as_float(w4[u] & 0xffff0000u) * f);
+                        const __half2 h2 = *reinterpret_cast<const __half2 *>(&hv[u]);
+                        qsum += __low2float(h2);
+                        qsum += __high2float(h2);
+                    }
                     *reinterpret_cast<uint4 *>(qh + (piece & 1) * NH * D * 2 + core_off(lane, 8 * c, C::Q_SR, C::Q_SC)) =
                         make_uint4(hv[0], hv[1], hv[2], hv[3]);
                 }
+                qpart[((piece & 3) * 4 + warp) * NH + lane] = qsum;  // 4 slots, as for the score factor
                 if (warp == 0 && lane == 0)
                     cred[4 + (piece & 3)] = a.q_scale_log2 * exp2i(-e);  // log2-domain factor of raw scores
                 __syncwarp();
@@ -742,10 +765,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const uint4 kv = kc[4 * half + jj];
-                    i8x4_to_f16x2x2(kv.x, kr[8 * jj + 0], kr[8 * jj + 1]);
-                    i8x4_to_f16x2x2(kv.y, kr[8 * jj + 2], kr[8 * jj + 3]);
-                    i8x4_to_f16x2x2(kv.z, kr[8 * jj + 4], kr[8 * jj + 5]);
-                    i8x4_to_f16x2x2(kv.w, kr[8 * jj + 6], kr[8 * jj + 7]);
+                    i8x4_to_f16x2x2_biased(kv.x, kr[8 * jj + 0], kr[8 * jj + 1]);
+                    i8x4_to_f16x2x2_biased(kv.y, kr[8 * jj + 2], kr[8 * jj + 3]);
+                    i8x4_to_f16x2x2_biased(kv.z, kr[8 * jj + 4], kr[8 * jj + 5]);
+                    i8x4_to_f16x2x2_biased(kv.w, kr[8 * jj + 6], kr[8 * jj + 7]);
                 }
                 tmem_st32(tmem + lane_base + C::K_COL + (uint32_t)buf * 64 + 32 * half, kr);
             }
@@ -928,6 +951,39 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             uint32_t sr[NHH];
             tmem_ld16(tmem + lane_base + C::S_COL + (uint32_t)buf * NH + NHH * hh, sr);
             tmem_wait_ld();
+            {
+                // take the K codes' bias off the scores: kBias * sum_d Q[h][d] per head, summed in
+                // a fixed order at the piece's first block (and kept for its later blocks)
+                float bq[NHH];
+                if (first) {
+                    const float4 *qp = reinterpret_cast<const float4 *>(qpart + (piece & 3) * 4 * NH + NHH * hh);
+#pragma unroll
+                    for (int q = 0; q < NHH / 4; ++q) {
+                        const float4 p0 = qp[q], p1 = qp[NH / 4 + q], p2 = qp[NH / 2 + q], p3 = qp[3 * NH / 4 + q];
+                        bq[4 * q] = kBias * (((p0.x + p1.x) + p2.x) + p3.x);
+                        bq[4 * q + 1] = kBias * (((p0.y + p1.y) + p2.y) + p3.y);
+                        bq[4 * q + 2] = kBias * (((p0.z + p1.z) + p2.z) + p3.z);
+                        bq[4 * q + 3] = kBias * (((p0.w + p1.w) + p2.w) + p3.w);
+                    }
+                    if ((sw & 3) == 0 && lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < NHH; ++j)
+                            bsum[NHH * hh + j] = bq[j];  // read from the next block on, after the barrier below
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < NHH / 4; ++q) {
+                        const float4 b4 = reinterpret_cast<const float4 *>(bsum + NHH * hh)[q];
+                        bq[4 * q] = b4.x;
+                        bq[4 * q + 1] = b4.y;
+                        bq[4 * q + 2] = b4.z;
+                        bq[4 * q + 3] = b4.w;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < NHH; ++j)
+                    sr[j] = __float_as_uint(__uint_as_float(sr[j]) - bq[j]);
+            }
             const float kg = ksv * gh;  // raw score -> log2 domain
             // a piece's first block always moves the references (they start at -inf)
             bool need = valid && (first || !(vsv <= exp2i(E_run)));
