@@ -16,23 +16,29 @@
 // call, so the workspace needs no zeroing.  In the whole-sequence mode CTA c
 // computes pair c alone and needs no workspace.
 //
-// Roles (9 warps, one CTA per SM):
-//   warps 0-3  converters.  Thread t owns token row t of every block.  Waits
-//              for its TMA boxes, converts the K codes to fp16 straight into
-//              tensor memory (the A operand of S^T = K Q^T), the V codes to
-//              fp16 in shared memory (the A operand of O^T += V^T P'), copies
-//              the scales, and refills its warp's two boxes of the ring.  At
-//              a pair's first block it also converts Q (loaded into registers
-//              one block ahead) into the B operand of S^T = K Q^T.
-//   warps 4-7  softmax.  Thread t reads token t's 32 scores from tensor
-//              memory, applies the K scale, exponentiates against a per-head
-//              reference maximum that only moves when a score exceeds it by
-//              more than 2^8 (then O is rescaled in tensor memory: rare), and
-//              writes P' = p * s_v * 2^(6-E) (fp16; 2^E a running power-of-two
-//              bound of the V scales, so P' stays below 64).  At a piece's
-//              last block it normalises O and stores the output or partial.
-//   warp 8     lane 0 issues every tcgen05.mma and commit; the warp owns the
-//              tensor-memory allocation.
+// Roles (14 warps, one CTA per SM):
+//   warps 0-3   converters.  Thread t owns token row t of every block.  Waits
+//               for its tile of the ring, converts the K codes to fp16 (kept
+//               with their exponent bias +1152) straight into tensor memory
+//               (the A operand of S^T = K Q^T) and the V codes to fp16 in
+//               place in the ring stage (the A operand of O^T += V^T P'), and
+//               copies the token's scales (landed with the codes) and
+//               validity into the block's scale slot.  At a piece's first
+//               block it also converts Q (bulk-copied a piece ahead) into the
+//               B operand of S^T = K Q^T, scaled by one exact power of two,
+//               and sums it per head for the bias.
+//   warps 4-11  softmax.  Thread (t, half) reads token t's 16 scores of its
+//               head half from tensor memory, takes the K bias off, applies
+//               the K scale, exponentiates against a per-head reference
+//               maximum that only moves when a score exceeds it by more than
+//               2^8 (then O is rescaled in tensor memory: rare), and writes
+//               P' = p * s_v * 2^(6-E) (fp16; 2^E a running power-of-two bound
+//               of the V scales, so P' stays below 2^14).  At a piece's last
+//               block it normalises O and stores the output or partial.
+//   warp 12     lane 0 issues every tcgen05.mma and commit; the warp owns the
+//               tensor-memory allocation.
+//   warp 13     TMA: block ids a block ahead, the codes and scales of each
+//               block into a ring stage once its O^T update has completed.
 //
 // Every int8 code is converted exactly once (exponent-bias trick, exact), the
 // scores and O accumulate in fp32 tensor memory, and every wait is bounded:
