@@ -54,7 +54,9 @@ class Setup:
 
 
 def build_caches(rng, seq_lens, page_size, head_dim, num_caches, shuffle=True, with_host_lens=True,
-                 pb: synth.PagedBatch | None = None, kv_scale: float = 1.0) -> Setup:
+                 pb: synth.PagedBatch | None = None, kv_scale: float = 1.0, kv_bits=None) -> Setup:
+    """Caches filled by kv_quant_append (GPU) and the oracle's quantiser (CPU) from the
+    same bf16 K/V rows: N(0, kv_scale^2) draws, or kv_bits[c] = (k, v) when given."""
     seq_lens = np.asarray(seq_lens, np.int32)
     pb = pb or synth.make_paged_batch(rng, seq_lens, page_size, shuffle=shuffle)
     cu = synth.cu_from_counts(seq_lens)
@@ -62,9 +64,12 @@ def build_caches(rng, seq_lens, page_size, head_dim, num_caches, shuffle=True, w
     batch = mk.Batch.from_host(pb.block_table, seq_lens, with_host_lens=with_host_lens)
     cu_dev = to_dev_i32(cu)
     gpu, ora, bits = [], [], []
-    for _ in range(num_caches):
-        k = synth.bf16_normal(rng, (T, head_dim), kv_scale)
-        v = synth.bf16_normal(rng, (T, head_dim), kv_scale)
+    for c in range(num_caches):
+        if kv_bits is not None:
+            k, v = kv_bits[c]
+        else:
+            k = synth.bf16_normal(rng, (T, head_dim), kv_scale)
+            v = synth.bf16_normal(rng, (T, head_dim), kv_scale)
         gc = mk.KVCache.empty(pb.num_blocks, page_size, head_dim)
         mk.kv_quant_append(gc, batch, cu_dev, T, to_dev_bf16(k), to_dev_bf16(v))
         oc = oracle.Cache.empty(pb.num_blocks, page_size, head_dim)

@@ -146,6 +146,27 @@ def test_decode_large_magnitudes_stay_finite():
     assert rel <= 5e-3 and np.abs(g - ref).max() <= 1e-2 * scale
 
 
+@pytest.mark.parametrize("k_offset", [1.0, 30.0])
+def test_decode_one_signed_queries_and_skewed_keys(k_offset):
+    """Queries whose 128 entries all share one sign and keys whose codes sit near
+    one end of the int8 range (a common offset ten times their spread): sum_d
+    Q[h][d] is as large as it gets, so the K conversion's bias (1152 per code,
+    taken off the scores in fp32) is at its largest against the scores it rides on."""
+    rng = np.random.default_rng(41)
+    d, page = 128, 64
+    lens = np.array([1, 129, 1500, 4096], np.int32)
+    T = int(lens.sum())
+    k = rng.standard_normal((T, d), dtype=np.float32) * np.float32(0.1 * k_offset) + np.float32(k_offset)
+    v = rng.standard_normal((T, d), dtype=np.float32)
+    s = build_caches(rng, lens, page, d, 1, kv_bits=[(synth.f32_to_bf16_bits(k), synth.f32_to_bf16_bits(v))])
+    for sign in (1.0, -1.0):
+        qf = (np.abs(rng.standard_normal((4, 32, d), dtype=np.float32)) + np.float32(0.5)) * np.float32(sign * 2.0)
+        q = synth.f32_to_bf16_bits(qf)
+        for window in (0, 1024):
+            out, ref = run_decode(s, q, window, num_splits=0)
+            assert_close(out, ref, f"one-signed q sign {sign} window {window} k_offset {k_offset}")
+
+
 def test_decode_is_deterministic():
     rng = np.random.default_rng(5)
     lens = rng.integers(1, 5000, size=16).astype(np.int32)
