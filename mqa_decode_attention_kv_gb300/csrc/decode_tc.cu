@@ -454,6 +454,28 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     const int cta = blockIdx.x;
     const bool balanced = a.persistent != 0;
 
+    // ---- set-up: barriers and tensor memory (no inputs needed: overlaps the length reads below)
+    if (tid == 0) {
+        for (int s = 0; s < 2 * RING; ++s) {
+            mbar_init(tfull + s, 1);
+            mbar_init(tfree + s, 1);
+        }
+        for (int s = 0; s < C::DEPTH; ++s) {
+            mbar_init(kready + s, 4);
+            mbar_init(vready + s, 4);
+            mbar_init(pready + s, 8);
+            mbar_init(sfull + s, 1);
+            mbar_init(odone + s, 1);
+        }
+        for (int s = 0; s < 2; ++s)
+            mbar_init(ofree + s, 8);
+        mbar_init(qfull, 1);
+        mbar_init(qfree, 4);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 12)
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
     // ---- this CTA's share of the (sequence, group, block) list
     if (balanced && a.batch <= C::THREADS) {
         // one pass (a sequence per thread): its blocks, the block-wide prefix and total
@@ -609,8 +631,15 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         a.merge_desc[(2 * cta) * 8] = -1;
         a.merge_desc[(2 * cta + 1) * 8] = -1;
     }
-    if (n <= 0)
-        return;  // uniform: nothing to compute
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (n <= 0) {  // uniform: nothing to compute
+        if (warp == 12)
+            tmem_dealloc(tmem, C::TMEM_COLS);
+        return;
+    }
     const long long list_first = share[0], list_n = share[1];
     const int Ge = (int)share[2];  // CTAs with a share (balanced mode)
     Cursor c0;
@@ -618,33 +647,6 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     c0.g = start_pos[1];
     c0.blk = start_pos[2];
     cursor_seek(c0, a);  // loads the shape of sequence c0.b (which has blocks)
-
-    // ---- set-up: barriers, tensor memory, the first RING blocks in flight
-    if (tid == 0) {
-        for (int s = 0; s < 2 * RING; ++s) {
-            mbar_init(tfull + s, 1);
-            mbar_init(tfree + s, 1);
-        }
-        for (int s = 0; s < C::DEPTH; ++s) {
-            mbar_init(kready + s, 4);
-            mbar_init(vready + s, 4);
-            mbar_init(pready + s, 8);
-            mbar_init(sfull + s, 1);
-            mbar_init(odone + s, 1);
-        }
-        for (int s = 0; s < 2; ++s)
-            mbar_init(ofree + s, 8);
-        mbar_init(qfull, 1);
-        mbar_init(qfree, 4);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 12)
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's tensor-memory lanes
     constexpr uint32_t IDESC_QK = umma_idesc_f16(128, NH, false, false);
 
