@@ -672,8 +672,9 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             const bool first = (i == 0) || cur.blk == 0;
             bool ok = wait_phase(tfull + 2 * r + my_tile, (uint32_t)(i / RING) & 1u, abort_flag);
             if (i >= C::DEPTH) {
-                // K buffer [buf] free once S^T(i-DEPTH) is done; scale slot [buf] once softmax(i-DEPTH) is
-                ok = ok && wait_phase(sfull + buf, phd(i - C::DEPTH), abort_flag);
+                // scale slot [buf] free once softmax(i-DEPTH) is done, and with it K buffer [buf]:
+                // the softmax warps arrive only after they saw S^T(i-DEPTH), which read K(i-DEPTH),
+                // complete, so this one wait orders the tensor core's reads before the stores below
                 ok = ok && wait_phase(pready + buf, phd(i - C::DEPTH), abort_flag);
             }
             if (first) {
