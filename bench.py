@@ -9,8 +9,10 @@ the 24 decode-attention calls in layer order (split-KV + combine where the
 planner chooses it).  Other workloads (--workload) time a single local layer,
 a single long-context global layer, or the prefix-reuse chunked prefill.
 
-Prints ONE JSON line (rank 0).  See the design doc for the accounting and the
-meaning of every field.
+Prints ONE JSON line (rank 0): the step's decode tokens/s as `value`, the
+decode kernel's HBM roofline (every call timed alone with L2 flushed before it),
+the same step through the public Python API with host buffers (`e2e`), and the
+CPU oracle's rate on a bounded sample of the workload (`cpu_baseline`).
 """
 from __future__ import annotations
 
@@ -242,30 +244,35 @@ def time_steps(fn, steps, flush_buf, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def cold_call_times(stack: DecodeStack, reps, flush_buf, stream):
-    """Device time of every attention call with L2 flushed before it: the
-    per-launch HBM roofline measurement.  Returns {layer: [ms, ...]}."""
+def cold_layer_times(stack: DecodeStack, reps, flush_buf, stream):
+    """Every layer of the step as its own timed segment with L2 flushed before
+    it: the append of the cache it is the first to read (if any), then its
+    decode call.  Returns ({layer: [segment ms]}, {layer: [decode-call ms]}):
+    the sum of the segments is a step whose every layer reads its KV from HBM;
+    the decode-call times are the per-launch HBM roofline measurement."""
     import torch
     sptr = stream.cuda_stream
-    res = {l: [] for l in range(stack.w.num_layers)}
+    seg = {l: [] for l in range(stack.w.num_layers)}
+    call = {l: [] for l in range(stack.w.num_layers)}
     evs = []
     with torch.cuda.stream(stream):
         for _ in range(reps):
             for l in range(stack.w.num_layers):
+                flush_l2(flush_buf)
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(stream)
                 c = stack.append_before.get(l)
                 if c is not None:
                     stack.append(c, sptr)
-                flush_l2(flush_buf)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                stack.attend(l, sptr)
                 e1.record(stream)
-                evs.append((l, e0, e1))
+                stack.attend(l, sptr)
+                e2.record(stream)
+                evs.append((l, e0, e1, e2))
     stream.synchronize()
-    for l, e0, e1 in evs:
-        res[l].append(e0.elapsed_time(e1))
-    return res
+    for l, e0, e1, e2 in evs:
+        seg[l].append(e0.elapsed_time(e2))
+        call[l].append(e1.elapsed_time(e2))
+    return seg, call
 
 
 def e2e_steps(stack: DecodeStack, steps, stream):
@@ -309,46 +316,62 @@ def e2e_steps(stack: DecodeStack, steps, stream):
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
+class OracleStack:
+    """The oracle (single-threaded C, fp64) set up on a bounded, seeded sample of
+    the workload's sequences: caches filled with their tokens, one query per
+    layer and one new K/V token per cache."""
+
+    def __init__(self, w: "synth.Workload", n_seqs: int, seed: int = 123):
+        import oracle
+        oracle.build()
+        self.oracle, self.w = oracle, w
+        rng = np.random.default_rng(w.seed)
+        lens_all = synth.seq_lens_for(w, rng)
+        pick = synth.sample_rows(np.random.default_rng(seed), len(lens_all), n_seqs)
+        self.lens = lens_all[pick]
+        self.pb = synth.make_paged_batch(rng, self.lens, w.page_size, shuffle=w.shuffle)
+        cu = synth.cu_from_counts(self.lens)
+        T = int(cu[-1])
+        d, H = w.head_dim, w.num_q_heads
+        self.caches = []
+        for _ in range(w.num_caches):
+            c = oracle.Cache.empty(self.pb.num_blocks, w.page_size, d)
+            oracle.quant_append(c, self.pb.block_table, self.lens, cu, synth.bf16_normal(rng, (T, d)),
+                                synth.bf16_normal(rng, (T, d)))
+            self.caches.append(c)
+        n = len(self.lens)
+        self.q = [synth.bf16_normal(rng, (n, H, d)) for _ in range(w.num_layers)]
+        self.kn = [synth.bf16_normal(rng, (n, d)) for _ in range(w.num_caches)]
+        self.vn = [synth.bf16_normal(rng, (n, d)) for _ in range(w.num_caches)]
+        self.cu_step = synth.cu_from_counts(np.ones(n))
+        first = {}
+        for l, c in enumerate(w.layer_map):
+            first.setdefault(c, l)
+        self.before = {l: c for c, l in first.items()}
+        self.scale = 1.0 / math.sqrt(d)
+        self.desc = (f"{n} of {w.batch} sequences (seeded sample, mean context {self.lens.mean():.0f}) "
+                     f"through all {w.num_layers} layers; one decode token each")
+
+    def step(self) -> float:
+        """One decode step of the sample (appends + every layer); returns seconds."""
+        w = self.w
+        t0 = time.perf_counter()
+        for l in range(w.num_layers):
+            c = self.before.get(l)
+            if c is not None:
+                self.oracle.quant_append(self.caches[c], self.pb.block_table, self.lens, self.cu_step, self.kn[c],
+                                         self.vn[c])
+            self.oracle.decode(self.caches[w.layer_map[l]], self.pb.block_table, self.lens, self.q[l], w.windows[l],
+                               self.scale)
+        return time.perf_counter() - t0
+
+
 def oracle_decode_sample(w: "synth.Workload", n_seqs: int, seed: int = 123):
-    """Time the oracle (single-threaded C, fp64) on a bounded sample of the
-    workload: n_seqs sequences drawn from the workload's length mix run through
-    every layer (append of the new token where a cache is first used, then
-    decode attention).  Returns (tokens/s, seconds, description)."""
-    import oracle
-    oracle.build()
-    rng = np.random.default_rng(w.seed)
-    lens_all = synth.seq_lens_for(w, rng)
-    pick = synth.sample_rows(np.random.default_rng(seed), len(lens_all), n_seqs)
-    lens = lens_all[pick]
-    pb = synth.make_paged_batch(rng, lens, w.page_size, shuffle=w.shuffle)
-    cu = synth.cu_from_counts(lens)
-    T = int(cu[-1])
-    d, H = w.head_dim, w.num_q_heads
-    caches = []
-    for _ in range(w.num_caches):
-        c = oracle.Cache.empty(pb.num_blocks, w.page_size, d)
-        oracle.quant_append(c, pb.block_table, lens, cu, synth.bf16_normal(rng, (T, d)),
-                            synth.bf16_normal(rng, (T, d)))
-        caches.append(c)
-    q = [synth.bf16_normal(rng, (len(lens), H, d)) for _ in range(w.num_layers)]
-    kn = [synth.bf16_normal(rng, (len(lens), d)) for _ in range(w.num_caches)]
-    vn = [synth.bf16_normal(rng, (len(lens), d)) for _ in range(w.num_caches)]
-    cu_step = synth.cu_from_counts(np.ones(len(lens)))
-    first = {}
-    for l, c in enumerate(w.layer_map):
-        first.setdefault(c, l)
-    before = {l: c for c, l in first.items()}
-    scale = 1.0 / math.sqrt(d)
-    t0 = time.perf_counter()
-    for l in range(w.num_layers):
-        c = before.get(l)
-        if c is not None:
-            oracle.quant_append(caches[c], pb.block_table, lens, cu_step, kn[c], vn[c])
-        oracle.decode(caches[w.layer_map[l]], pb.block_table, lens, q[l], w.windows[l], scale)
-    dt = time.perf_counter() - t0
-    desc = (f"{len(lens)} of {w.batch} sequences (seeded sample, mean context {lens.mean():.0f}) "
-            f"through all {w.num_layers} layers; one decode token each")
-    return len(lens) / dt, dt, desc
+    """Time one oracle step on a bounded sample of the workload: n_seqs
+    sequences through every layer.  Returns (tokens/s, seconds, description)."""
+    st = OracleStack(w, n_seqs, seed)
+    dt = st.step()
+    return len(st.lens) / dt, dt, st.desc
 
 
 class PrefillWorkload:
@@ -455,17 +478,24 @@ def describe(w: "synth.Workload", lens) -> str:
 
 
 def run_reference(args, w):
-    """Reference arm: the CPU oracle, as it stands, on the host cores."""
+    """Reference arm: the CPU oracle, as it stands, on the host cores.  Each
+    step is one decode step of a bounded sample of the workload (the same
+    --ref-seqs sequences every step): W untimed warm-up steps, then K timed."""
     rank, world, _ = rank_info()
     if rank != 0:
         return
-    n = args.cpu_seqs
-    val, dt, desc = oracle_decode_sample(w, n)
+    st = OracleStack(w, args.ref_seqs)
+    for _ in range(args.warmup):
+        st.step()
+    times = [st.step() for _ in range(args.steps)]
+    dt = sum(times) / len(times)
+    val = len(st.lens) / dt
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": describe(w, synth.seq_lens_for(w, np.random.default_rng(w.seed)))},
-            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "data": "synthetic", "config": {"workload": describe(w, synth.seq_lens_for(w, np.random.default_rng(w.seed))),
+                                            "sample_per_step": st.desc},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": st.desc},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -508,9 +538,11 @@ def run_decode(args, w):
 
     # eager step (no graph) for reference
     eager = time_steps(lambda: stack.step(sptr), max(3, min(args.steps, 10)), flush, stream)
-    # per-call cold-L2 timings: the roofline of the decode kernel (+ its split combine)
-    cold = cold_call_times(stack, args.roofline_reps, flush, stream)
+    # every layer with L2 flushed before it: the step with all KV from HBM, and the
+    # per-call roofline of the decode kernel (+ the kernel merging cut pairs)
+    seg, cold = cold_layer_times(stack, args.roofline_reps, flush, stream)
     cold_ms = {l: statistics.mean(v) for l, v in cold.items()}
+    seg_ms = sum(statistics.mean(v) for v in seg.values())
     achieved = sum(stack.bytes_per_layer) / (sum(cold_ms.values()) * 1e6)
     loc = [l for l in range(w.num_layers) if w.windows[l] > 0]
     glo = [l for l in range(w.num_layers) if w.windows[l] == 0]
@@ -545,9 +577,16 @@ def run_decode(args, w):
         "vs_baseline": None, "dtype": "i8kv-f16mma-f32acc", "data": "synthetic",
         "config": {"workload": describe(w, stack.lens), "global_batch": B * world,
                    "seq_len": f"{w.len_kind} {w.len_values}", "parallelism": f"replicas x{world}",
-                   "l2": "L2 flushed (512 MB read) before every timed step; inputs (KV read per step) exceed L2",
+                   "l2": ("L2 flushed (512 MB read) before every timed step, outside the timed interval.  Inside "
+                          "the step the second of two adjacent layers that share a cache finds part of it in L2 "
+                          "(nothing runs between them), so kv_gbps is not an HBM figure; step_layers_cold and "
+                          "roofline time every layer with L2 flushed before it"),
                    "timing": "CUDA graph of the whole step, replayed; CUDA events on the launching stream",
                    "kv_bytes_per_step": kv_bytes, "kv_gbps": kv_bytes / (ms * 1e6)},
+        "step_layers_cold": {"ms_per_step": seg_ms, "tokens_per_s": world * B / (seg_ms / 1000.0),
+                             "kv_gbps": kv_bytes / (seg_ms * 1e6),
+                             "how": "sum over the 24 layers of (append if any + decode call), each timed alone "
+                                    "with L2 flushed before it (eager launches)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": "decode attention call (the decode kernel + the kernel merging pairs cut between "
@@ -662,7 +701,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="stack24_b128", choices=sorted(synth.CONFIGS))
     ap.add_argument("--roofline-reps", type=int, default=3)
-    ap.add_argument("--cpu-seqs", type=int, default=32, help="sequences in the oracle's timed sample")
+    ap.add_argument("--cpu-seqs", type=int, default=32, help="sequences in the cpu_baseline's timed sample")
+    ap.add_argument("--ref-seqs", type=int, default=4,
+                    help="sequences per step of the reference arm (the oracle on the host cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",

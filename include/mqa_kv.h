@@ -185,7 +185,8 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
  * allocate device memory (for example code running while a framework captures
  * a CUDA graph and forbids new allocations, serving loops whose memory budget
  * is reserved up front, or plugins with no access to the process's allocator).
- * The paper has no counterpart to this call; it exists for those callers.
+ * The pages this library follows describe no counterpart to this call; it
+ * exists for those callers.
  *
  * Same arguments and results as mqa_decode_attn, minus workspace.  Split-KV
  * partials go to one library-owned device array of 32 MiB that every GPU which
@@ -196,7 +197,9 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
  * shares the one array: calls whose GPU work overlaps (other streams, other
  * threads) race and must be serialised by the caller.  The first call on a
  * device looks up the array's device address; make that first call before any
- * stream capture. */
+ * stream capture.  The address is kept for the life of the process: do not use
+ * this entry point on a device after cudaDeviceReset (or after its primary
+ * context was destroyed), because later calls would reuse the old address. */
 int mqa_decode_attn_noalloc(const mqa_kv_cache *caches, int32_t num_caches, const int32_t *layer_to_kv,
                             int32_t num_layers, int32_t layer, int32_t window, const mqa_batch *batch,
                             const void *q, void *out, int32_t num_q_heads, float sm_scale, int32_t num_splits,

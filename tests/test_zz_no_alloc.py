@@ -13,9 +13,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 import mqa_decode_attention_kv_gb300 as mk
-from gpu_common import MAX_ABS, REL_L2, build_caches, errors, to_dev_bf16
+from gpu_common import MAX_ABS, REL_L2, assert_close, build_caches, errors, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +39,8 @@ def test_noalloc_matches_workspace_entry_point_twice(window, lens):
     d, H = 128, 32
     s = build_caches(rng, np.array(lens, np.int32), 64, d, 1)
     for call in range(2):  # the scratch array keeps the previous call's contents
-        q = to_dev_bf16(synth.bf16_normal(rng, (len(lens), H, d)))
+        q_bits = synth.bf16_normal(rng, (len(lens), H, d))
+        q = to_dev_bf16(q_bits)
         ref = mk.mqa_decode_attn(s.gpu_caches, [0], 0, window, s.batch, q, sm_scale=1.0 / math.sqrt(d))
         got = noalloc_call(s, q, window, 0, H, d)
         forced = noalloc_call(s, q, window, 4, H, d)
@@ -46,6 +48,10 @@ def test_noalloc_matches_workspace_entry_point_twice(window, lens):
         for g in (got, forced):
             max_abs, rel, _ = errors(g, ref.float().cpu().numpy().astype(np.float64))
             assert max_abs <= MAX_ABS and rel <= REL_L2, f"call {call}: max_abs={max_abs:.2e} rel={rel:.2e}"
+        # and directly against the oracle
+        exact, _ = oracle.decode(s.ora_caches[0], s.pb.block_table, s.seq_lens, q_bits, window, 1.0 / math.sqrt(d))
+        assert_close(got, exact, f"noalloc call {call} vs oracle")
+        assert_close(forced, exact, f"noalloc (4 splits) call {call} vs oracle")
 
 
 def test_noalloc_rejects_split_counts_beyond_its_scratch():
