@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
                                                      int32_t num_q_heads, __nv_bfloat16 *__restrict__ out)
 {
     constexpr int V = D / 32;  // fp32 elements per lane (4 or 2)
+    griddep_wait();  // the partials of the decode kernel before it on the stream
+    griddep_launch_dependents();
     __shared__ float red[kCombineWarps];
     __shared__ float part[kCombineWarps][D];
     __shared__ float dens[kCombineWarps];
@@ -125,10 +127,10 @@ cudaError_t launch_combine(const float *o_partial, const float *lse, int32_t bat
         return cudaSuccess;
     dim3 grid((unsigned)num_q_heads, (unsigned)batch);
     if (head_dim == 128)
-        combine_kernel<128><<<grid, 32 * kCombineWarps, 0, s>>>(o_partial, lse, num_splits, num_q_heads, out);
-    else
-        combine_kernel<64><<<grid, 32 * kCombineWarps, 0, s>>>(o_partial, lse, num_splits, num_q_heads, out);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<128>, grid, dim3(32 * kCombineWarps), 0, s, o_partial, lse, num_splits,
+                          num_q_heads, out);
+    return launch_pdl(combine_kernel<64>, grid, dim3(32 * kCombineWarps), 0, s, o_partial, lse, num_splits,
+                      num_q_heads, out);
 }
 
 }  // namespace mqa

@@ -17,8 +17,20 @@ namespace mqa {
 constexpr int kTileTokens = 64;   // tokens per pipeline stage
 constexpr int kChunkTokens = 16;  // rows per TMA box (a box never crosses a page: P in {16, 64})
 constexpr int kChunksPerTile = kTileTokens / kChunkTokens;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
+// Bounded waits.  A pipeline wait (one role waiting for another) gives up after
+// kWaitLimitNs and reports MQA_DEV_TIMEOUT; a drain (a CTA that gave up waiting
+// for its own copies and MMAs in flight before it leaves) uses kDrainLimitNs.
+// MQA_TEST_WAIT_LIMIT_NS builds a test-only library whose pipeline waits give
+// up almost at once, to exercise the abort path; drains keep their limit.
+#ifdef MQA_TEST_WAIT_LIMIT_NS
+constexpr unsigned long long kWaitLimitNs = MQA_TEST_WAIT_LIMIT_NS;
+constexpr uint32_t kTryWaitSuspendNs = 0;
+#else
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTryWaitSuspendNs = 1000000;  // let a waiting thread sleep instead of spinning
+#endif
+constexpr unsigned long long kDrainLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kDrainSuspendNs = 1000000;
 
 // ---------------------------------------------------------------- addressing
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -78,6 +90,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Whether phase `parity` of `bar` has completed (does not wait).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.  Returns false
 // on timeout (the caller reports it and leaves); never spins forever.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
@@ -92,6 +131,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (global_timer_ns() - t0 > kWaitLimitNs)
             return false;
     }
+}
+
+// The same with the drain limit: a CTA that is leaving early waits this long for
+// its own asynchronous copies and MMAs before it gives up.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait_hint(bar, parity, kDrainSuspendNs))
+        return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_hint(bar, parity, kDrainSuspendNs))
+                return true;
+        if (global_timer_ns() - t0 > kDrainLimitNs)
+            return false;
+    }
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels are launched with programmatic stream serialisation: a kernel may
+// start while its predecessor on the stream is still running.  griddep_wait()
+// blocks until the predecessor grid has completed and its memory is visible;
+// every kernel calls it before its first access to global memory.
+// griddep_launch_dependents() lets the successor start its own set-up early.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMA

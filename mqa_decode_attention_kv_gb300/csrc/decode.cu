@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(128, 3) decode_kernel(const __grid_constant__ 
 {
     using C = DecodeCfg<D, HT>;
     constexpr int S = C::STAGES, BPW = C::BPW, HG = C::HG, NT = C::NT;
+    griddep_wait();  // the previous kernel's writes (cache slots, q, tickets) are visible from here
+    griddep_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint32_t *box_ok = reinterpret_cast<uint32_t *>(base + C::OFF_OK);
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(128, 3) decode_kernel(const __grid_constant__ 
             set_status(a.dev_status, MQA_DEV_TIMEOUT);
             for (int s = 0; s < S * kChunksPerTile; ++s)
                 if (issued[s] >= 0)
-                    mbar_wait_bounded(mbar + s, (uint32_t)(issued[s] / S) & 1u);
+                    mbar_wait_drain(mbar + s, (uint32_t)(issued[s] / S) & 1u);
         }
         return;
     }
@@ -613,8 +615,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s)
         attr_set.store(1, std::memory_order_release);
     }
     dim3 grid(a.num_splits, a.batch, (a.num_q_heads + HT - 1) / HT);
-    decode_kernel<D, HT><<<grid, 128, C::SMEM_BYTES, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_kernel<D, HT>, grid, dim3(128), C::SMEM_BYTES, s, a);
 }
 
 template <int D, int HT>

@@ -1,49 +1,60 @@
 // Decode attention on the 5th-generation tensor cores (tcgen05), head_dim 128,
-// groups of 32 query heads: one persistent, warp-specialised kernel.
+// groups of 32 query heads: one persistent kernel with worker warpgroups.
 //
 // Work.  The call's (sequence b, head group g, 128-token key block) triples
 // form one list, ordered by b, then g, then block.  In the balanced mode CTA c
 // of the first G' = min(G, N) CTAs takes the contiguous share
 // [c*N/G', (c+1)*N/G') of the N list entries (never empty), so every CTA
-// streams the same number of blocks (+-1) whatever the length mix and
-// its pipeline runs across sequence boundaries without draining.  A piece of
-// a (b, g) pair that lies inside one share is the whole pair: its output is
+// streams the same number of blocks (+-1) whatever the length mix and its
+// pipeline runs across sequence boundaries without draining.  A piece of a
+// (b, g) pair that lies inside one share is the whole pair: its output is
 // written directly (bf16).  A pair cut by share boundaries leaves an fp32
 // partial (O, lse) per piece in slot 0 (the share's first piece) or 1 (its
-// last) of the CTA that computed it, and the CTA holding its last piece
-// writes a merge descriptor; a second kernel merges every cut pair, a CTA per
-// (pair, 8 heads).  Each CTA rewrites both of its descriptor slots on every
-// call, so the workspace needs no zeroing.  In the whole-sequence mode CTA c
-// computes pair c alone and needs no workspace.
+// last) of the CTA that computed it, and the CTA holding its last piece writes
+// a merge descriptor; a second kernel merges every cut pair, a CTA per (pair,
+// 8 heads).  Each CTA rewrites both of its descriptor slots on every call, so
+// the workspace needs no zeroing.  In the whole-pair mode CTA c computes pair
+// c alone and needs no workspace.
 //
-// Roles (14 warps, one CTA per SM):
-//   warps 0-3   converters.  Thread t owns token row t of every block.  Waits
-//               for its tile of the ring, converts the K codes to fp16 (kept
-//               with their exponent bias +1152) straight into tensor memory
-//               (the A operand of S^T = K Q^T) and the V codes to fp16 in
-//               place in the ring stage (the A operand of O^T += V^T P'), and
-//               copies the token's scales (landed with the codes) and
-//               validity into the block's scale slot.  At a piece's first
-//               block it also converts Q (bulk-copied a piece ahead) into the
-//               B operand of S^T = K Q^T, scaled by one exact power of two,
-//               and sums it per head for the bias.
-//   warps 4-11  softmax.  Thread (t, half) reads token t's 16 scores of its
-//               head half from tensor memory, takes the K bias off, applies
-//               the K scale, exponentiates against a per-head reference
-//               maximum that only moves when a score exceeds it by more than
-//               2^8 (then O is rescaled in tensor memory: rare), and writes
-//               P' = p * s_v * 2^(6-E) (fp16; 2^E a running power-of-two bound
-//               of the V scales, so P' stays below 2^14).  At a piece's last
-//               block it normalises O and stores the output or partial.
-//   warp 12     lane 0 issues every tcgen05.mma and commit; the warp owns the
-//               tensor-memory allocation.
-//   warp 13     TMA: block ids a block ahead, the codes and scales of each
-//               block into a ring stage once its O^T update has completed.
+// Roles (12 warps, one CTA per SM):
+//   warps 0-7   two worker warpgroups.  Worker group w takes the CTA's blocks
+//               i with i % 2 == w, whole: thread t owns token row t (= tensor
+//               memory lane t).  Per block it converts the K codes to fp16
+//               (kept with their exponent bias +1152) straight into its K
+//               buffer in tensor memory (the A operand of S^T = K Q^T), the V
+//               codes to fp16 in place in the ring stage (the A operand of
+//               O^T += V^T P'), then reads its token's 32 scores, takes the K
+//               bias off, applies the K scale and writes
+//               P' = 2^(score - ref) * s_v * 2^(6-E) (fp16) for the MMA.  Each
+//               group keeps its own per-head reference maxima (moved only when
+//               a score passes them by more than 2^8, or at the group's first
+//               block of a piece), its own power-of-two bound 2^E of the V
+//               scales, its own row sums and its own O accumulator in tensor
+//               memory; the group that computes a piece's last block merges
+//               both groups' (O, ref, sum, E) into the piece's result.  The
+//               group that computes a piece's first block converts its Q
+//               (bulk-copied a piece ahead) into the B operand of S^T, scaled
+//               by one exact power of two, and sums it per head for the bias.
+//   warps 8-11  the control warpgroup (its registers go to the workers):
+//               lane 0 of warp 8 (group 0) and of warp 10 (group 1) issue
+//               their group's tcgen05.mma and commits, S^T(i) as soon as K(i)
+//               is in tensor memory and O^T_w += V^T(i) P'(i) once P'(i) is
+//               written; warp 8 owns the tensor-memory allocation.  Warp 9
+//               is the TMA producer: block ids a block ahead, the codes and
+//               scales of each block into a ring stage once the O^T update
+//               that read the stage's previous block has completed.  Warp 11
+//               idles.
 //
 // Every int8 code is converted exactly once (exponent-bias trick, exact), the
-// scores and O accumulate in fp32 tensor memory, and every wait is bounded:
-// a wait that runs out raises a CTA-wide abort flag that makes all roles
-// leave, and the call reports MQA_DEV_TIMEOUT.
+// scores and O accumulate in fp32 tensor memory.  Every wait is bounded: a
+// wait that runs out raises a CTA-wide abort flag; every role then leaves at
+// its next exit point (the worker groups all together, at a barrier that ORs
+// the flag), copies and MMAs still in flight are drained first, and the call
+// reports MQA_DEV_TIMEOUT.
+//
+// The kernel is launched with programmatic stream serialisation: barrier and
+// tensor-memory set-up overlap the previous kernel on the stream, and every
+// global access comes after griddep_wait().
 #include <atomic>
 #include <cfloat>
 #include <math.h>
@@ -61,35 +72,44 @@ struct TcCfg {
     static constexpr int NH = 32;                    // heads per group (MMA N)
     static constexpr int BT = 128;                   // tokens per block (M of S^T, K of O^T)
     static constexpr int BOXES = BT / kChunkTokens;  // 8 TMA boxes of 16 tokens
+    static constexpr int NW = 2;                     // worker warpgroups
     static constexpr int RING = 5;                   // ring stages (codes in flight, then fp16 V)
-    static constexpr int DEPTH = 3;                  // blocks in flight between roles (S, K, P, scales)
-    static constexpr int THREADS = 448;              // 4 converter + 8 softmax warps, MMA warp, TMA warp
+    // a control warpgroup after the workers: the MMA warp, the TMA warp and two idle warps
+    static constexpr int MMA_WARP = 4 * NW, TMA_WARP = 4 * NW + 1;
+    static constexpr int THREADS = 32 * (4 * NW + 4);
+    // registers per thread: at launch (one CTA per SM), then moved from the control group to
+    // the workers with setmaxnreg; the split must fit what the CTA was launched with
+    static constexpr int REG_LAUNCH = (65536 / THREADS) / 8 * 8;
+    static constexpr int REG_CTRL = 88;
+    static constexpr int REG_WORK = ((REG_LAUNCH * THREADS - 128 * REG_CTRL) / (128 * NW)) / 8 * 8;
     static constexpr int CODES = BT * D;             // int8 bytes of K (or V) of a block
     static constexpr int STAGE = 2 * CODES;          // K codes, V codes; then fp16 V in place
     // shared memory (offsets from a 1024-aligned base)
     static constexpr int OFF_RING = 0;
-    static constexpr int OFF_QH = OFF_RING + RING * STAGE;      // [2] fp16 Q [32 h][128 d], core layout (piece parity)
-    static constexpr int OFF_QRAW = OFF_QH + 2 * NH * D * 2;    // bf16 Q [32 h][128 d] as copied (next piece)
-    static constexpr int OFF_PH = OFF_QRAW + NH * D * 2;        // [DEPTH] fp16 P' [128 tok][32 h], core layout
-    static constexpr int OFF_SC = OFF_PH + DEPTH * BT * NH * 2;  // [DEPTH][3][128] fp32: K scale, V scale, valid
-    static constexpr int OFF_RED = OFF_SC + DEPTH * 3 * BT * 4;  // softmax group: [4 warps][32] + [4] fp32
-    static constexpr int OFF_MREF = OFF_RED + 160 * 4;          // softmax group: reference maxima [32], factors [32]
-    static constexpr int OFF_CRED = OFF_MREF + 64 * 4;          // converter group: [4] fp32, gh[4]
-    static constexpr int OFF_OK = OFF_CRED + 16 * 4;            // [RING][8] box arrived
-    static constexpr int OFF_SCL = OFF_OK + RING * BOXES * 4;   // [RING][2][128] fp32 K, V token scales (TMA)
-    static constexpr int OFF_QB = OFF_SCL + RING * 2 * BT * 4;  // [4 pieces][4 warps][32] fp32 partial sums of Q
-    static constexpr int OFF_BS = OFF_QB + 4 * 4 * NH * 4;      // [32] fp32 K bias of the piece's scores
-    static constexpr int OFF_MISC = OFF_BS + NH * 4;            // tmem base, abort flag, start position
+    static constexpr int OFF_QH = OFF_RING + RING * STAGE;     // [2 slots] fp16 Q [32 h][128 d], core layout
+    static constexpr int OFF_QRAW = OFF_QH + 2 * NH * D * 2;   // bf16 Q [32 h][128 d] as copied (next piece)
+    static constexpr int OFF_PH = OFF_QRAW + NH * D * 2;       // [NW] fp16 P' [128 tok][32 h], core layout
+    static constexpr int OFF_SCL = OFF_PH + NW * BT * NH * 2;  // [RING][2][128] fp32 K, V token scales (TMA)
+    static constexpr int OFF_OK = OFF_SCL + RING * 2 * BT * 4;  // [RING][8] box arrived
+    // per worker group: red [4 warps][32], vred [4], mref [32], fac [NW][32]
+    static constexpr int WG_RED = 0, WG_VRED = 512, WG_MREF = 528, WG_FAC = 656;
+    static constexpr int WG_BYTES = (WG_FAC + NW * NH * 4 + 15) / 16 * 16;
+    static constexpr int OFF_WG = OFF_OK + RING * BOXES * 4;
+    // per piece slot (2): bias [32], gh, then per group: ref [32], sum [32], E
+    static constexpr int SL_BIAS = 0, SL_GH = 128, SL_GRP = 144, SL_GRP_BYTES = 272;
+    static constexpr int SLOT_BYTES = (SL_GRP + NW * SL_GRP_BYTES + 15) / 16 * 16;
+    static constexpr int OFF_SLOT = OFF_WG + NW * WG_BYTES;
+    static constexpr int OFF_MISC = OFF_SLOT + 2 * SLOT_BYTES;  // tmem base, abort flag, start position, share
     static constexpr int OFF_MBAR = OFF_MISC + 256;
-    static constexpr int NBAR = 4 * RING + 5 * DEPTH + 4;  // tiles, 5 x DEPTH hand-offs, O free [2], Q full / free
+    static constexpr int NBAR = 3 * RING + 5 * NW + 7;
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
-    // tensor memory columns: S^T [DEPTH][32], O^T [2][32], fp16 K [DEPTH][64]
+    // tensor memory columns: S^T [NW][32], O^T [NW][2][32], fp16 K [NW][64]
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t S_COL = 0, O_COL = DEPTH * NH, K_COL = O_COL + 2 * NH;
+    static constexpr uint32_t S_COL = 0, O_COL = NW * NH, K_COL = O_COL + 2 * NW * NH;
     // core-matrix strides (bytes): V rows = tokens, Q rows = heads, P rows = tokens.  The fp16
-    // V of converter warp w's tokens 32w .. 32w+31 overwrites the 8 KB of codes they came
-    // from: 8-token groups 0, 1 of the warp at K-half offset 4096w, groups 2, 3 at V-half
-    // offset 4096w, each group 16 core matrices (8 d each) of 128 B.
+    // V of token group warp j (tokens 32j .. 32j+31) overwrites the 8 KB of codes they came
+    // from: 8-token groups 0, 1 of the warp at K-half offset 4096j, groups 2, 3 at V-half
+    // offset 4096j, each group 16 core matrices (8 d each) of 128 B.
     static constexpr uint32_t V_SR = 16 * 128;  // next 8 tokens (inside a 16-token MMA step)
     static constexpr uint32_t V_SC = 128;       // next 8 d
     static constexpr uint32_t Q_SR = 16 * 128;  // next 8 heads
@@ -98,38 +118,41 @@ struct TcCfg {
     static constexpr uint32_t P_SC = 128;       // next 8 heads
 };
 static_assert(TcCfg::SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(TcCfg::RING >= TcCfg::NW + 1, "the ring must hold every group's block and one more");
+static_assert(TcCfg::NW <= 3, "the control warpgroup has one MMA issuer per worker group, besides the TMA warp");
+static_assert(TcCfg::REG_WORK <= 256 && TcCfg::REG_WORK >= TcCfg::REG_LAUNCH &&
+                  128 * (TcCfg::NW * TcCfg::REG_WORK + TcCfg::REG_CTRL) <= TcCfg::REG_LAUNCH * TcCfg::THREADS,
+              "register split within the launch allocation");
 // 128-byte-swizzled TMA destinations and descriptor bases on 1024 B; bulk copies, vector
 // loads and stores on 16 B; mbarriers on 8 B
 static_assert(TcCfg::OFF_RING % 1024 == 0 && TcCfg::STAGE % 1024 == 0 && TcCfg::OFF_QH % 1024 == 0 &&
-                  TcCfg::OFF_PH % 1024 == 0, "1024-byte alignment");
-static_assert(TcCfg::OFF_QRAW % 16 == 0 && TcCfg::OFF_SC % 16 == 0 && TcCfg::OFF_RED % 16 == 0 &&
-                  TcCfg::OFF_MREF % 16 == 0 && TcCfg::OFF_CRED % 16 == 0 && TcCfg::OFF_OK % 16 == 0 &&
-                  TcCfg::OFF_SCL % 16 == 0 && TcCfg::OFF_QB % 16 == 0 && TcCfg::OFF_BS % 16 == 0 &&
-                  TcCfg::OFF_MISC % 16 == 0 && TcCfg::OFF_MBAR % 8 == 0,
+                  TcCfg::OFF_PH % 1024 == 0,
+              "1024-byte alignment");
+static_assert(TcCfg::OFF_QRAW % 16 == 0 && TcCfg::OFF_SCL % 16 == 0 && TcCfg::OFF_OK % 16 == 0 &&
+                  TcCfg::OFF_WG % 16 == 0 && TcCfg::WG_BYTES % 16 == 0 && TcCfg::WG_MREF % 16 == 0 &&
+                  TcCfg::WG_FAC % 16 == 0 && TcCfg::OFF_SLOT % 16 == 0 && TcCfg::SLOT_BYTES % 16 == 0 &&
+                  TcCfg::SL_GRP % 16 == 0 && TcCfg::SL_GRP_BYTES % 16 == 0 && TcCfg::OFF_MISC % 16 == 0 &&
+                  TcCfg::OFF_MBAR % 8 == 0,
               "16-byte alignment");
-static_assert(TcCfg::K_COL + TcCfg::DEPTH * 64 <= TcCfg::TMEM_COLS, "tensor memory budget");
-
-// Mbarrier wait with a suspend hint: a waiting warp sleeps until the phase
-// completes instead of polling (eight warps polling would crowd the shared-
-// memory pipe that the converters, the TMA and the tensor core use).
-__device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) { return mbar_try_wait(bar, parity); }
+static_assert(TcCfg::K_COL + TcCfg::NW * 64 <= TcCfg::TMEM_COLS, "tensor memory budget");
 
 // Bounded wait that also gives up once another role has raised the abort
 // flag; a wait that runs out raises it.  Returns false when giving up.
-__device__ __noinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag);
+__device__ __forceinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag);
 
 __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
 {
-    return mbar_poll(bar, parity) || wait_phase_slow(bar, parity, abort_flag);
+    return mbar_try_wait(bar, parity) || wait_phase_slow(bar, parity, abort_flag);
 }
 
-// The polling loop, out of line: the many wait sites stay small.
-__device__ __noinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+// The polling loop (inlined: a called function could not serve warpgroups that
+// run with different register counts).
+__device__ __forceinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
 {
     const unsigned long long t0 = global_timer_ns();
     while (true) {
         for (int i = 0; i < 16; ++i)
-            if (mbar_poll(bar, parity))
+            if (mbar_try_wait(bar, parity))
                 return true;
         if (*abort_flag)
             return false;
@@ -163,33 +186,6 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool pred)
     return r != 0;
 }
 
-// Parity of the phase of a two-buffer hand-off barrier that carries item i.
-__device__ __forceinline__ uint32_t ph2(int i) { return (uint32_t)(i >> 1) & 1u; }
-// Buffer and phase parity of block i on a DEPTH-buffer hand-off (i >= 0).
-__device__ __forceinline__ int bufd(int i) { return i % TcCfg::DEPTH; }
-__device__ __forceinline__ uint32_t phd(int i) { return (uint32_t)(i / TcCfg::DEPTH) & 1u; }
-
-// Reduce 16 per-head values over the 32 lanes of a warp with 16 shuffles (the
-// butterfly below over each half-warp, then one exchange between the halves):
-// lane L returns the reduction of head L % 16.  v is consumed.
-template <bool MAX>
-__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lane)
-{
-#pragma unroll
-    for (int s = 8; s >= 1; s >>= 1) {
-        const bool up = (lane & s) != 0;
-#pragma unroll
-        for (int k = 0; k < s; ++k) {
-            const float send = up ? v[k] : v[k + s];
-            const float keep = up ? v[k + s] : v[k];
-            const float got = __shfl_xor_sync(0xffffffffu, send, s);
-            v[k] = MAX ? fmaxf(keep, got) : keep + got;
-        }
-    }
-    const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
-    return MAX ? fmaxf(v[0], other) : v[0] + other;
-}
-
 // Reduce 32 per-head values over the 32 lanes of a warp with 31 shuffles (a
 // butterfly that halves the values each lane keeps at every step): lane L
 // returns the reduction of head L.  v is consumed.
@@ -218,18 +214,6 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "{\n\t.reg .pred pa;\n\tsetp.ne.u32 pa, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
 }
 
 // Key blocks of a sequence of length L: the 64-token tiles from the one
@@ -353,7 +337,7 @@ __device__ __forceinline__ void issue_block(const DecodeArgs &a, const Cursor &p
 // Four codes (byte i = code c_i) -> lo = {c0, c1} + kBias, hi = {c2, c3} + kBias as f16x2,
 // exact: the exponent-bias conversion (0x64xx = 1024 + byte, on the codes offset by 128)
 // without its final subtraction.  K enters S^T = K Q^T this way; the bias adds
-// kBias * sum_d Q[h][d] to every score of head h, which the softmax warps take off in fp32.
+// kBias * sum_d Q[h][d] to every score of head h, which the worker groups take off in fp32.
 constexpr float kBias = 1152.f;
 __device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
@@ -364,39 +348,6 @@ __device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t w, uint32_t &lo,
 
 // Shared-memory descriptor plus a byte offset (the address field counts 16 B).
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
-
-// O^T += V^T(j) P'(j) for block j into the O buffer of its piece (MMA thread).
-// Returns false when a wait gave up.
-__device__ __forceinline__ bool issue_pv(int j, uint32_t first_bits, int &piece, int &n_pv, uint32_t tmem,
-                                         uint64_t vdesc0, uint64_t pdesc0, uint64_t *pready, uint64_t *vready,
-                                         uint64_t *ofree, uint64_t *odone, uint64_t *sfree, volatile int *abort_flag)
-{
-    using C = TcCfg;
-    constexpr uint32_t IDESC_PV = umma_idesc_f16(128, C::NH, true, true);
-    const int jb = bufd(j);
-    if (!wait_phase(pready + jb, phd(j), abort_flag) || !wait_phase(vready + jb, phd(j), abort_flag))
-        return false;
-    const bool first = (first_bits >> (j & 31)) & 1u;
-    if (first) {
-        ++piece;
-        // the O buffer of piece - 2 must have been read by its epilogue
-        if (piece >= 2 && !wait_phase(ofree + (piece & 1), ph2(piece - 2), abort_flag))
-            return false;
-    }
-    tc_fence_after();
-    const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * C::NH;
-    // V: fp16 in place in ring stage j % RING; 16-token step kk = token groups 2kk, 2kk+1 of
-    // converter warp kk / 2, in the K half (kk even) or the V half (kk odd)
-    const uint64_t vd = desc_add(vdesc0, (j % C::RING) * C::STAGE), pd = desc_add(pdesc0, jb * C::BT * C::NH * 2);
-#pragma unroll
-    for (int kk = 0; kk < C::BT / 16; ++kk)
-        umma_f16(tmem + o_col, desc_add(vd, (kk & 1) * C::CODES + (kk >> 1) * 4096), desc_add(pd, kk * 2 * C::P_SR),
-                 IDESC_PV, !first || kk > 0);
-    umma_commit(odone + jb);
-    umma_commit(sfree + (j % C::RING));  // the stage's V is read: the TMA warp may refill it
-    ++n_pv;
-    return true;
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -411,42 +362,57 @@ __device__ __forceinline__ size_t merge_row(int c_lo, int s, int slot_lo, int jh
     return (size_t)(2 * (c_lo + s) + (s == 0 ? slot_lo : 0)) * TcCfg::NH + jh;
 }
 
+// Whether worker group w computes a block of the piece whose blocks are list
+// positions [i0, i0 + nb) (block i goes to group i % NW).
+__device__ __forceinline__ bool group_in_piece(int w, int i0, int nb)
+{
+    return nb >= TcCfg::NW || ((w - i0 % TcCfg::NW + TcCfg::NW) % TcCfg::NW) < nb;
+}
+
 }  // namespace
+
+// The CTA-wide barrier of the teardown.  Every role ends with its own copy of
+// the teardown (the roles run with different register counts and never rejoin).
+__device__ __forceinline__ void bar_all() { asm volatile("bar.sync 0;" ::: "memory"); }
+
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(TcCfg::REG_WORK));
+}
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(TcCfg::REG_CTRL));
+}
 
 __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __grid_constant__ DecodeArgs a)
 {
     using C = TcCfg;
-    constexpr int D = C::D, NH = C::NH, RING = C::RING, BT = C::BT;
-    constexpr int BAR_SM = 1;  // named barrier of the softmax warps
+    constexpr int D = C::D, NH = C::NH, RING = C::RING, BT = C::BT, NW = C::NW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *qh = base + C::OFF_QH;
     uint8_t *qraw = base + C::OFF_QRAW;
     uint8_t *ph = base + C::OFF_PH;
-    float *sc = reinterpret_cast<float *>(base + C::OFF_SC);
-    float *red = reinterpret_cast<float *>(base + C::OFF_RED);
-    float *mref = reinterpret_cast<float *>(base + C::OFF_MREF);  // [32] per-head reference (log2 domain)
-    float *ofac_s = mref + NH;                                     // [32] per-head O rescale factors
-    float *cred = reinterpret_cast<float *>(base + C::OFF_CRED);
     uint32_t *box_ok = reinterpret_cast<uint32_t *>(base + C::OFF_OK);
     float *scl = reinterpret_cast<float *>(base + C::OFF_SCL);  // [RING][2][128] token scales, with the codes
-    float *qpart = reinterpret_cast<float *>(base + C::OFF_QB);  // [4][4][32] per-warp sums of the fp16 Q
-    float *bsum = reinterpret_cast<float *>(base + C::OFF_BS);   // [32] kBias * sum_d Q of the piece
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 4);
+    volatile int *q_issued = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);  // raw Q copies issued
     int *start_pos = reinterpret_cast<int *>(base + C::OFF_MISC + 16);          // b, g, blk, n
     long long *share = reinterpret_cast<long long *>(base + C::OFF_MISC + 32);  // first entry, N, CTAs
     static_assert(32 + 3 * 8 <= 64, "misc layout");
     uint64_t *tfull = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][2] tile codes landed (TMA)
-    uint64_t *tfree = tfull + 2 * RING;         // [RING] stage free: O^T of its block done (tensor core)
-    uint64_t *kready = tfree + 2 * RING;        // [DEPTH] K in tensor memory, scales, Q (4 converter warps)
-    uint64_t *vready = kready + C::DEPTH;       // [DEPTH] fp16 V in shared memory     (4 converter warps)
-    uint64_t *pready = vready + C::DEPTH;       // [DEPTH] P' written, S read          (8 softmax warps)
-    uint64_t *sfull = pready + C::DEPTH;        // [DEPTH] S^T = K Q^T done            (tensor core)
-    uint64_t *odone = sfull + C::DEPTH;         // [DEPTH] O^T += V^T P' done          (tensor core)
-    uint64_t *ofree = odone + C::DEPTH;         // [2] a piece's O read by its epilogue (8 softmax warps)
-    uint64_t *qfull = ofree + 2;                // raw Q of the next piece landed      (bulk copy)
-    uint64_t *qfree = qfull + 1;                // raw Q read by every converter warp  (4 converter warps)
+    uint64_t *tfree = tfull + 2 * RING;  // [RING] stage free: O^T of its block done   (tensor core)
+    uint64_t *kready = tfree + RING;     // [NW] K in tensor memory (+ Q of a new piece) (4 warps)
+    uint64_t *vready = kready + NW;      // [NW] fp16 V in shared memory                (4 warps)
+    uint64_t *pready = vready + NW;      // [NW] P' written, S read                     (4 warps)
+    uint64_t *sfull = pready + NW;       // [NW] S^T = K Q^T done                       (tensor core)
+    uint64_t *odone = sfull + NW;        // [NW] O^T += V^T P' done                     (tensor core)
+    uint64_t *qready = odone + NW;       // [2] the piece slot's Q, bias, factor ready  (4 warps)
+    uint64_t *pdone = qready + 2;        // [2] every group is done with the piece      (4 NW warps)
+    uint64_t *sfree = pdone + 2;         // [2] the piece's epilogue read slot and O    (4 warps)
+    uint64_t *qfull = sfree + 2;         // raw Q of the next piece landed              (bulk copy)
+    static_assert(3 * C::RING + 5 * C::NW + 7 == C::NBAR, "barrier count");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int groups = (a.num_q_heads + NH - 1) / NH;
@@ -454,32 +420,45 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     const int cta = blockIdx.x;
     const bool balanced = a.persistent != 0;
 
-    // ---- set-up: barriers and tensor memory (no inputs needed: overlaps the length reads below)
+    // ---- set-up: barriers and tensor memory (touches no global memory: overlaps the previous kernel)
     if (tid == 0) {
-        for (int s = 0; s < 2 * RING; ++s) {
+        for (int s = 0; s < 2 * RING; ++s)
             mbar_init(tfull + s, 1);
+        for (int s = 0; s < RING; ++s)
             mbar_init(tfree + s, 1);
+        for (int w = 0; w < NW; ++w) {
+            mbar_init(kready + w, 4);
+            mbar_init(vready + w, 4);
+            mbar_init(pready + w, 4);
+            mbar_init(sfull + w, 1);
+            mbar_init(odone + w, 1);
         }
-        for (int s = 0; s < C::DEPTH; ++s) {
-            mbar_init(kready + s, 4);
-            mbar_init(vready + s, 4);
-            mbar_init(pready + s, 8);
-            mbar_init(sfull + s, 1);
-            mbar_init(odone + s, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(qready + s, 4);
+            mbar_init(pdone + s, 4 * NW);
+            mbar_init(sfree + s, 4);
         }
-        for (int s = 0; s < 2; ++s)
-            mbar_init(ofree + s, 8);
         mbar_init(qfull, 1);
-        mbar_init(qfree, 4);
         *abort_flag = 0;
+        *q_issued = 0;
         fence_mbar_init();
     }
-    if (warp == 12)
+    if (warp == C::MMA_WARP)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
+    if (warp == C::TMA_WARP && lane == 0) {
+        const bool p64 = a.page_size == kTileTokens;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.k_map64 : &a.k_map))
+                     : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.v_map64 : &a.v_map))
+                     : "memory");
+    }
+    // the previous kernel's writes (the cache slot just appended, q, out, the workspace) are visible from here
+    griddep_wait();
+    griddep_launch_dependents();
     // ---- this CTA's share of the (sequence, group, block) list
+    int *wsum = reinterpret_cast<int *>(base + C::OFF_WG);  // scratch of the scans (worker-group area)
     if (balanced && a.batch <= C::THREADS) {
         // one pass (a sequence per thread): its blocks, the block-wide prefix and total
-        int *wsum = reinterpret_cast<int *>(red);
         int nb = 0;
         if (tid < a.batch) {
             int tf, lo;
@@ -525,7 +504,6 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         }
         __syncthreads();
     } else if (balanced) {
-        int *wsum = reinterpret_cast<int *>(red);
         // pass 1: blocks per group over all sequences; sequences without blocks
         // (invalid length) get a zero output from CTA b % G and a status bit
         long long mine = 0;
@@ -599,7 +577,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         }
         __syncthreads();
     } else {
-        // whole-sequence mode: CTA c computes (sequence c / groups, group c % groups)
+        // whole-pair mode: CTA c computes (sequence c / groups, group c % groups)
         if (tid == 0) {
             const int bb = cta / groups, gg = cta % groups;
             int tf, lo;
@@ -632,11 +610,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         a.merge_desc[(2 * cta + 1) * 8] = -1;
     }
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // also: the scans' scratch is free for the worker groups
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (n <= 0) {  // uniform: nothing to compute
-        if (warp == 12)
+        if (warp == C::MMA_WARP)
             tmem_dealloc(tmem, C::TMEM_COLS);
         return;
     }
@@ -647,197 +625,451 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     c0.g = start_pos[1];
     c0.blk = start_pos[2];
     cursor_seek(c0, a);  // loads the shape of sequence c0.b (which has blocks)
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's tensor-memory lanes
-    constexpr uint32_t IDESC_QK = umma_idesc_f16(128, NH, false, false);
+    // registers: the control warpgroup gives most of its share to the worker groups
+    if (warp < 4 * NW)
+        regs_inc();
+    else
+        regs_dec();
 
-    if (warp < 4) {
-        // ================================================================ converters
-        const int tok = tid;  // token row of every block = tensor-memory lane
-        const int my_tile = warp >> 1;            // warps 0, 1 read tile 0 of a block; warps 2, 3 tile 1
-        Cursor cur = c0;
-        int q_issued = 0;
-        {
-            // the first piece's Q (bf16, 32 heads x 256 B, contiguous)
-            if (warp == 0 && lane == 0) {
-                mbar_arrive_expect_tx(qfull, NH * D * 2);
-                bulk_load(qraw, a.q + ((size_t)c0.b * a.num_q_heads + c0.g * NH) * D, NH * D * 2, qfull);
-            }
-            q_issued = 1;
+    if (warp < 4 * NW) {
+        // ================================================================ worker groups
+        const int w = warp >> 2, wj = warp & 3;
+        const int tok = 32 * wj + lane;                        // token row of every block = tensor-memory lane
+        const uint32_t lane_base = (uint32_t)(32 * wj) << 16;  // this warp's tensor-memory lanes
+        const int BAR_WG = 1 + w;                              // named barrier of this group
+        uint8_t *wg = base + C::OFF_WG + w * C::WG_BYTES;
+        float *red = reinterpret_cast<float *>(wg + C::WG_RED);    // [4 warps][32]
+        float *vred = reinterpret_cast<float *>(wg + C::WG_VRED);  // [4]
+        float *mref = reinterpret_cast<float *>(wg + C::WG_MREF);  // [32] reference maxima (log2 domain)
+        float *fac = reinterpret_cast<float *>(wg + C::WG_FAC);    // [NW][32] factors
+        uint8_t *pw = ph + w * BT * NH * 2;                        // this group's P'
+        const uint32_t s_col = C::S_COL + (uint32_t)w * NH, k_col = C::K_COL + (uint32_t)w * 64;
+        if (w == 0 && wj == 0 && lane == 0) {
+            // the first piece's Q (bf16, 32 heads x 256 B, contiguous): group 0 converts it
+            *q_issued = 1;
+            mbar_arrive_expect_tx(qfull, NH * D * 2);
+            bulk_load(qraw, a.q + ((size_t)c0.b * a.num_q_heads + c0.g * NH) * D, NH * D * 2, qfull);
         }
-        int piece = -1;
-        int i = 0;
-        for (; i < n; ++i) {
-            const int r = i % RING, buf = bufd(i);
-            uint8_t *st = base + C::OFF_RING + r * C::STAGE;
+        Cursor cur = c0;
+        float l_acc[NH];  // this token's sum of p per head, for the current piece
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+            l_acc[h] = 0.f;
+        const float *bias = nullptr;  // kBias * sum_d Q[h][d] of the current piece (its slot)
+        int E_run = -100;       // running power-of-two bound of the V scales (group-uniform)
+        float gh = 0.f;         // log2-domain factor of the raw scores of the piece
+        int piece = -1, piece_i0 = 0;
+        bool piece_from_start = false, took = false;  // took: this group computed a block of the piece
+        int jw = 0;                                   // blocks this group computed so far
+        bool ok = true;
+        for (int i = 0; i < n; ++i) {
             const bool first = (i == 0) || cur.blk == 0;
-            bool ok = wait_phase(tfull + 2 * r + my_tile, (uint32_t)(i / RING) & 1u, abort_flag);
-            if (i >= C::DEPTH) {
-                // scale slot [buf] free once softmax(i-DEPTH) is done, and with it K buffer [buf]:
-                // the softmax warps arrive only after they saw S^T(i-DEPTH), which read K(i-DEPTH),
-                // complete, so this one wait orders the tensor core's reads before the stores below
-                ok = ok && wait_phase(pready + buf, phd(i - C::DEPTH), abort_flag);
-            }
+            const bool last = (i == n - 1) || cur.blk == cur.nblk - 1;
+            const bool mine = (i % NW) == w;
             if (first) {
-                ok = ok && wait_phase(qfull, (uint32_t)(piece + 1) & 1u, abort_flag);  // this piece's raw Q
-                if (i >= 2)  // fp16 Q buffer (piece parity) was last read by piece-2's S^T, done by S^T(i-2)
-                    ok = ok && wait_phase(sfull + bufd(i - 2), phd(i - 2), abort_flag);
-            }
-            if (!__all_sync(0xffffffffu, ok))
-                break;
-            tc_fence_after();
-            if (first) {
-                // ---- Q of this piece, scaled by one power of two 2^e (exact in fp16): lane =
-                // head; pass 1 takes the max over the 32 x 128 values (chunks read in a
-                // lane-rotated order: no bank conflicts), pass 2 converts this warp's d range
                 ++piece;
-                const uint8_t *qrow = qraw + lane * D * 2;
-                float m = 0.f;
+                piece_i0 = i;
+                piece_from_start = cur.blk == 0;
+                took = false;
+                const int s = piece & 1;
+                uint8_t *slot = base + C::OFF_SLOT + s * C::SLOT_BYTES;
+                if (mine) {
+                    // ---- this group converts the piece's Q into slot s (free once piece-2's
+                    // epilogue read it) and sums it per head; lane = head
+                    if (piece >= 2)
+                        ok &= wait_phase(sfree + s, (uint32_t)((piece - 2) >> 1) & 1u, abort_flag);
+                    ok &= wait_phase(qfull, (uint32_t)piece & 1u, abort_flag);
+                    const uint8_t *qrow = qraw + lane * D * 2;
+                    float m = 0.f;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * ((k + lane) & 15));
-                    const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+                    for (int k = 0; k < 16; ++k) {
+                        const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * ((k + lane) & 15));
+                        const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[t] << 16)),
-                                           fabsf(__uint_as_float(w4[t] & 0xffff0000u))));
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                int e = 0;
-                if (m > 0.f && isfinite(m)) {
-                    int x;
-                    frexpf(m, &x);
-                    e = min(120, max(-120, 14 - x));
-                }
-                const float f = exp2i(e);
-                float qsum = 0.f;  // this warp's d range of head `lane`, as the tensor core sees it
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int c = 4 * warp + ((t + lane) & 3);  // 8-d chunk: d = 8c .. 8c+7
-                    const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * c);
-                    const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
-                    uint32_t hv[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        hv[u] = pack_half2(__uint_as_float(w4[u] << 16) * f, __uint_as_float(w4[u] & 0xffff0000u) * f);
-                        const __half2 h2 = *reinterpret_cast<const __half2 *>(&hv[u]);
-                        qsum += __low2float(h2);
-                        qsum += __high2float(h2);
+                        for (int t = 0; t < 4; ++t)
+                            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[t] << 16)),
+                                               fabsf(__uint_as_float(w4[t] & 0xffff0000u))));
                     }
-                    *reinterpret_cast<uint4 *>(qh + (piece & 1) * NH * D * 2 + core_off(lane, 8 * c, C::Q_SR, C::Q_SC)) =
-                        make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                }
-                qpart[((piece & 3) * 4 + warp) * NH + lane] = qsum;  // 4 slots, as for the score factor
-                if (warp == 0 && lane == 0)
-                    cred[4 + (piece & 3)] = a.q_scale_log2 * exp2i(-e);  // log2-domain factor of raw scores
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(qfree);  // this warp has read the raw Q
-                // the next piece's Q, once every warp has read this one (only if this CTA has it)
-                const int i_next = i + (cur.nblk - cur.blk);
-                if (warp == 0 && i_next < n) {
-                    Cursor nx = cur;
-                    nx.blk = cur.nblk - 1;
-                    cursor_next(nx, a, groups);
-                    if (!__all_sync(0xffffffffu, wait_phase(qfree, (uint32_t)piece & 1u, abort_flag)))
-                        break;
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(qfull, NH * D * 2);
-                        bulk_load(qraw, a.q + ((size_t)nx.b * a.num_q_heads + nx.g * NH) * D, NH * D * 2, qfull);
-                    }
-                    ++q_issued;
-                }
-            }
-            // ---- this token's K codes (all chunks loaded before the conversion)
-            uint4 kc[D / 16];
-            {
-                const uint8_t *krow = st + tok * D;
 #pragma unroll
-                for (int j = 0; j < D / 16; ++j)
-                    kc[j] = *reinterpret_cast<const uint4 *>(krow + ((uint32_t)(j ^ (tok & 7)) << 4));
+                    for (int off = 16; off > 0; off >>= 1)
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                    int e = 0;
+                    if (m > 0.f && isfinite(m)) {
+                        int x;
+                        frexpf(m, &x);
+                        e = min(120, max(-120, 14 - x));
+                    }
+                    const float f = exp2i(e);
+                    float qsum = 0.f;  // this warp's d range of head `lane`, as the tensor core sees it
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int c = 4 * wj + ((t + lane) & 3);  // 8-d chunk: d = 8c .. 8c+7
+                        const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * c);
+                        const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+                        uint32_t hv[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            hv[u] = pack_half2(__uint_as_float(w4[u] << 16) * f,
+                                               __uint_as_float(w4[u] & 0xffff0000u) * f);
+                            const __half2 h2 = *reinterpret_cast<const __half2 *>(&hv[u]);
+                            qsum += __low2float(h2);
+                            qsum += __high2float(h2);
+                        }
+                        *reinterpret_cast<uint4 *>(qh + s * NH * D * 2 + core_off(lane, 8 * c, C::Q_SR, C::Q_SC)) =
+                            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    }
+                    red[wj * NH + lane] = qsum;
+                    fence_proxy_async();  // fp16 Q for the tensor core; raw Q reads before its next copy
+                    named_bar(BAR_WG, 128);
+                    if (wj == 0) {
+                        float *sb = reinterpret_cast<float *>(slot + C::SL_BIAS);
+                        sb[lane] = kBias * (((red[lane] + red[NH + lane]) + red[2 * NH + lane]) + red[3 * NH + lane]);
+                        if (lane == 0)
+                            *reinterpret_cast<float *>(slot + C::SL_GH) = a.q_scale_log2 * exp2i(-e);
+                        // the next piece's Q, now that every warp of the group has read this one
+                        const int i_next = i + (cur.nblk - cur.blk);
+                        if (lane == 0 && i_next < n && ok && !*abort_flag) {
+                            Cursor nx = cur;
+                            nx.blk = cur.nblk - 1;
+                            cursor_next(nx, a, groups);
+                            *q_issued = *q_issued + 1;  // before the arrival that publishes it
+                            mbar_arrive_expect_tx(qfull, NH * D * 2);
+                            bulk_load(qraw, a.q + ((size_t)nx.b * a.num_q_heads + nx.g * NH) * D, NH * D * 2, qfull);
+                        }
+                    }
+                    named_bar(BAR_WG, 128);  // red reuse; the slot's bias and factor written
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(qready + s);
+                } else {
+                    ok &= wait_phase(qready + s, (uint32_t)(piece >> 1) & 1u, abort_flag);
+                }
+                // this piece's Q factor and bias (the slot stays until the piece's epilogue)
+                gh = *reinterpret_cast<const float *>(slot + C::SL_GH);
+                bias = reinterpret_cast<const float *>(slot + C::SL_BIAS);
             }
-            {
+            if (mine) {
+                // ============================================ block i: K, V, softmax
+                const int r = i % RING;
+                const int pj = jw & 1;  // phase parity of this group's per-block barriers
+                uint8_t *st = base + C::OFF_RING + r * C::STAGE;
+                ok &= wait_phase(tfull + 2 * r + (wj >> 1), (uint32_t)(i / RING) & 1u, abort_flag);
+                tc_fence_after();
+                const uint8_t *crow = st + tok * D;  // this token's codes (K, then V at + CODES)
                 const int pos = (cur.t_first + 2 * cur.blk) * kTileTokens + tok;
                 const bool fetched = box_ok[r * C::BOXES + (tok >> 4)] != 0;
                 const bool valid = fetched && pos >= cur.lo && pos < cur.L;
-                const float *sr = scl + r * 2 * BT;  // landed with the codes
-                float *scb = sc + buf * 3 * BT;
-                scb[tok] = fetched ? sr[tok] : 0.f;
-                scb[BT + tok] = fetched ? sr[BT + tok] : 0.f;
-                scb[2 * BT + tok] = valid ? 1.f : 0.f;
-            }
-            // ---- K: 128 codes -> fp16 pairs in tensor memory (lane tok, 64 columns)
+                const float ksv = fetched ? scl[r * 2 * BT + tok] : 0.f;
+                const float vsv = fetched ? scl[r * 2 * BT + BT + tok] : 0.f;
+                // ---- K: 128 codes -> fp16 pairs in tensor memory (lane tok, 64 columns); the
+                // group's K buffer was last read by S^T of its previous block, which it waited for
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t kr[32];
+                for (int half = 0; half < 2; ++half) {
+                    uint4 kc[4];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const uint4 kv = kc[4 * half + jj];
-                    i8x4_to_f16x2x2_biased(kv.x, kr[8 * jj + 0], kr[8 * jj + 1]);
-                    i8x4_to_f16x2x2_biased(kv.y, kr[8 * jj + 2], kr[8 * jj + 3]);
-                    i8x4_to_f16x2x2_biased(kv.z, kr[8 * jj + 4], kr[8 * jj + 5]);
-                    i8x4_to_f16x2x2_biased(kv.w, kr[8 * jj + 6], kr[8 * jj + 7]);
+                    for (int jj = 0; jj < 4; ++jj)
+                        kc[jj] = *reinterpret_cast<const uint4 *>(crow + ((uint32_t)((4 * half + jj) ^ (tok & 7)) << 4));
+                    uint32_t kr[32];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint4 kv = kc[jj];
+                        i8x4_to_f16x2x2_biased(kv.x, kr[8 * jj + 0], kr[8 * jj + 1]);
+                        i8x4_to_f16x2x2_biased(kv.y, kr[8 * jj + 2], kr[8 * jj + 3]);
+                        i8x4_to_f16x2x2_biased(kv.z, kr[8 * jj + 4], kr[8 * jj + 5]);
+                        i8x4_to_f16x2x2_biased(kv.w, kr[8 * jj + 6], kr[8 * jj + 7]);
+                    }
+                    tmem_st32(tmem + lane_base + k_col + 32 * half, kr);
                 }
-                tmem_st32(tmem + lane_base + C::K_COL + (uint32_t)buf * 64 + 32 * half, kr);
-            }
-            tmem_wait_st();
-            fence_proxy_async();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(kready + buf);
-            // ---- V: fp16 in place over this warp's 8 KB of codes in stage r (every lane's
-            // rows are in registers once the warp passes the barrier): the MN-major A operand
-            // of O^T += V^T P', token group g = lane / 8 of the warp at (g < 2 ? K half :
-            // V half) + 4096 warp + 2048 (g % 2), row lane % 8 of its 16 core matrices.
-            uint4 vc[D / 16];
-            {
-                const uint8_t *vrow = st + C::CODES + tok * D;
+                // this token's V codes, in flight while the K stores complete
+                uint4 vc[D / 16];
 #pragma unroll
                 for (int j = 0; j < D / 16; ++j)
-                    vc[j] = *reinterpret_cast<const uint4 *>(vrow + ((uint32_t)(j ^ (tok & 7)) << 4));
-            }
-            __syncwarp();
-            {
-                const int g = lane >> 3;
-                uint8_t *vb = st + (g >> 1) * C::CODES + warp * 4096 + (g & 1) * 2048 + (lane & 7) * 16;
+                    vc[j] = *reinterpret_cast<const uint4 *>(crow + C::CODES + ((uint32_t)(j ^ (tok & 7)) << 4));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(kready + w);
+                // ---- V: fp16 in place over this warp's 8 KB of codes in stage r (every lane's
+                // rows are in registers): the MN-major A operand of O^T += V^T P', token group
+                // g = lane / 8 of the warp at (g < 2 ? K half : V half) + 4096 wj + 2048 (g % 2),
+                // row lane % 8 of its 16 core matrices
+                __syncwarp();
+                {
+                    const int g = lane >> 3;
+                    uint8_t *vb = st + (g >> 1) * C::CODES + wj * 4096 + (g & 1) * 2048 + (lane & 7) * 16;
 #pragma unroll
-                for (int j = 0; j < D / 16; ++j) {
-                    uint32_t v8[8];
-                    i8x4_to_f16x2x2(vc[j].x, v8[0], v8[1]);
-                    i8x4_to_f16x2x2(vc[j].y, v8[2], v8[3]);
-                    i8x4_to_f16x2x2(vc[j].z, v8[4], v8[5]);
-                    i8x4_to_f16x2x2(vc[j].w, v8[6], v8[7]);
-                    *reinterpret_cast<uint4 *>(vb + (2 * j) * C::V_SC) = make_uint4(v8[0], v8[1], v8[2], v8[3]);
-                    *reinterpret_cast<uint4 *>(vb + (2 * j + 1) * C::V_SC) = make_uint4(v8[4], v8[5], v8[6], v8[7]);
+                    for (int j = 0; j < D / 16; ++j) {
+                        uint32_t v8[8];
+                        i8x4_to_f16x2x2(vc[j].x, v8[0], v8[1]);
+                        i8x4_to_f16x2x2(vc[j].y, v8[2], v8[3]);
+                        i8x4_to_f16x2x2(vc[j].z, v8[4], v8[5]);
+                        i8x4_to_f16x2x2(vc[j].w, v8[6], v8[7]);
+                        *reinterpret_cast<uint4 *>(vb + (2 * j) * C::V_SC) = make_uint4(v8[0], v8[1], v8[2], v8[3]);
+                        *reinterpret_cast<uint4 *>(vb + (2 * j + 1) * C::V_SC) = make_uint4(v8[4], v8[5], v8[6], v8[7]);
+                    }
                 }
+                // O^T of this group's previous block done: its P' buffer and O are free, and the MMA
+                // thread has consumed that block's vready / pready phases (no phase can be lapped)
+                if (jw >= 1)
+                    ok &= wait_phase(odone + w, (uint32_t)(pj ^ 1), abort_flag);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(vready + w);
+                // ---- scores of this token: S^T(i) row tok, 32 heads
+                ok &= wait_phase(sfull + w, (uint32_t)pj, abort_flag);
+                tc_fence_after();
+                uint32_t sr[NH];
+                tmem_ld32(tmem + lane_base + s_col, sr);
+                tmem_wait_ld();
+                const float kg = ksv * gh;  // raw score -> log2 domain
+                float x[NH];
+                float dmax = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < NH / 4; ++q) {
+                    const float4 b4 = reinterpret_cast<const float4 *>(bias)[q];
+                    x[4 * q] = (__uint_as_float(sr[4 * q]) - b4.x) * kg;
+                    x[4 * q + 1] = (__uint_as_float(sr[4 * q + 1]) - b4.y) * kg;
+                    x[4 * q + 2] = (__uint_as_float(sr[4 * q + 2]) - b4.z) * kg;
+                    x[4 * q + 3] = (__uint_as_float(sr[4 * q + 3]) - b4.w) * kg;
+                }
+#pragma unroll
+                for (int q = 0; q < NH / 4; ++q) {
+                    const float4 m4 = reinterpret_cast<const float4 *>(mref)[q];
+                    dmax = fmaxf(dmax, fmaxf(fmaxf(x[4 * q] - m4.x, x[4 * q + 1] - m4.y),
+                                             fmaxf(x[4 * q + 2] - m4.z, x[4 * q + 3] - m4.w)));
+                }
+                // a group's first block of a piece always moves the references (they start at -inf)
+                const bool need = !took || (valid && (!(dmax <= 8.f) || !(vsv <= exp2i(E_run))));
+                ok &= *abort_flag == 0;
+                if (named_bar_or(BAR_WG, 128, need || !ok)) {
+                    if (named_bar_or(BAR_WG, 128, !ok))
+                        break;  // abort: the whole group leaves here together
+                    // rare: move the references to the block maxima (and the V-scale bound)
+                    {
+                        float mv[NH];
+#pragma unroll
+                        for (int h = 0; h < NH; ++h)
+                            mv[h] = valid ? x[h] : -INFINITY;
+                        red[wj * NH + lane] = warp_transpose_reduce<true>(mv, lane);  // head lane's warp max
+                    }
+                    float vm = valid ? vsv : 0.f;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                    if (lane == 0)
+                        vred[wj] = vm;
+                    named_bar(BAR_WG, 128);
+                    if (wj == 0) {
+                        const int h = lane;
+                        const float bm = fmaxf(fmaxf(red[h], red[NH + h]), fmaxf(red[2 * NH + h], red[3 * NH + h]));
+                        const float mo = took ? mref[h] : -INFINITY;
+                        const float mn = fmaxf(mo, bm);
+                        mref[h] = mn;
+                        fac[h] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
+                    }
+                    const float vmax = fmaxf(fmaxf(vred[0], vred[1]), fmaxf(vred[2], vred[3]));
+                    named_bar(BAR_WG, 128);
+                    const int E_new = max(took ? E_run : -100, ceil_log2_pow(vmax));
+                    const float escale = took ? exp2i(max(E_run - E_new, -126)) : 1.f;
+                    if (took) {
+                        // this group's O of the piece (its previous O^T update is done, waited
+                        // above): row d = tok, 32 heads
+                        const uint32_t o_col = C::O_COL + (uint32_t)(w * 2 + (piece & 1)) * NH;
+                        uint32_t orr[NH];
+                        tmem_ld32(tmem + lane_base + o_col, orr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < NH / 4; ++q) {
+                            const float4 f4 = reinterpret_cast<const float4 *>(fac)[q];
+                            l_acc[4 * q] *= f4.x;
+                            l_acc[4 * q + 1] *= f4.y;
+                            l_acc[4 * q + 2] *= f4.z;
+                            l_acc[4 * q + 3] *= f4.w;
+                            orr[4 * q] = __float_as_uint(__uint_as_float(orr[4 * q]) * (f4.x * escale));
+                            orr[4 * q + 1] = __float_as_uint(__uint_as_float(orr[4 * q + 1]) * (f4.y * escale));
+                            orr[4 * q + 2] = __float_as_uint(__uint_as_float(orr[4 * q + 2]) * (f4.z * escale));
+                            orr[4 * q + 3] = __float_as_uint(__uint_as_float(orr[4 * q + 3]) * (f4.w * escale));
+                        }
+                        tmem_st32(tmem + lane_base + o_col, orr);
+                        tmem_wait_st();
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < NH; ++h)
+                            l_acc[h] = 0.f;
+                    }
+                    E_run = E_new;
+                    named_bar(BAR_WG, 128);  // red, vred and fac are reused
+                }
+                took = true;
+                // ---- P' = 2^(score - ref) * s_v * 2^(6-E) as fp16: row tok of this group's P'
+                const float vf = valid ? vsv * exp2i(6 - E_run) : 0.f;
+#pragma unroll
+                for (int q = 0; q < NH / 8; ++q) {
+                    const float4 ma = reinterpret_cast<const float4 *>(mref)[2 * q];
+                    const float4 mb = reinterpret_cast<const float4 *>(mref)[2 * q + 1];
+                    const float mq[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int h0 = 8 * q + 2 * k;
+                        const float p0 = valid ? fast_exp2(x[h0] - mq[2 * k]) : 0.f;
+                        const float p1 = valid ? fast_exp2(x[h0 + 1] - mq[2 * k + 1]) : 0.f;
+                        l_acc[h0] += p0;
+                        l_acc[h0 + 1] += p1;
+                        pk[k] = pack_half2(p0 * vf, p1 * vf);
+                    }
+                    *reinterpret_cast<uint4 *>(pw + core_off(tok, 8 * q, C::P_SR, C::P_SC)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(pready + w);
+                ++jw;
             }
-            // vready[buf] may take block i's arrivals only once the MMA thread has consumed
-            // block i-DEPTH's phase (O^T(i-DEPTH) done): else its wait on that phase could be lapped
-            if (i >= C::DEPTH && !__all_sync(0xffffffffu, wait_phase(odone + buf, phd(i - C::DEPTH), abort_flag))) {
-                ++i;
-                break;
+            if (last) {
+                // ============================================ end of the piece
+                const int s = piece & 1;
+                uint8_t *slot = base + C::OFF_SLOT + s * C::SLOT_BYTES;
+                if (took) {
+                    // this group's last O^T update of the piece has completed (its issuer's commit):
+                    // after pdone, the epilogue may read every group's O
+                    ok &= wait_phase(odone + w, (uint32_t)((jw - 1) & 1), abort_flag);
+                    // this group's row sums over its 128 tokens (l_acc is consumed: the next piece
+                    // starts from zero), its references and E
+                    red[wj * NH + lane] = warp_transpose_reduce<false>(l_acc, lane);
+                    named_bar(BAR_WG, 128);
+                    if (wj == 0) {
+                        float *gs = reinterpret_cast<float *>(slot + C::SL_GRP + w * C::SL_GRP_BYTES);
+                        gs[lane] = mref[lane];
+                        gs[NH + lane] = ((red[lane] + red[NH + lane]) + red[2 * NH + lane]) + red[3 * NH + lane];
+                        if (lane == 0)
+                            reinterpret_cast<int *>(gs)[2 * NH] = E_run;
+                    }
+                    named_bar(BAR_WG, 128);  // red reuse
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(pdone + s);
+                if (mine) {
+                    // this group computed the piece's last block: merge every group's share (every
+                    // participant's O^T updates completed before it arrived on pdone)
+                    ok &= wait_phase(pdone + s, (uint32_t)(piece >> 1) & 1u, abort_flag);
+                    tc_fence_after();
+                    const int nb = i - piece_i0 + 1;
+                    const bool whole_pair = piece_from_start && cur.blk == cur.nblk - 1;
+                    const int oslot = piece_i0 == 0 ? 0 : 1;
+                    if (wj == 0) {
+                        // head lane: the merged reference, sum, and every group's output factor
+                        const int h = lane;
+                        float M = -INFINITY;
+#pragma unroll
+                        for (int u = 0; u < NW; ++u)
+                            if (group_in_piece(u, piece_i0, nb))
+                                M = fmaxf(M, reinterpret_cast<const float *>(slot + C::SL_GRP + u * C::SL_GRP_BYTES)[h]);
+                        // (a group without a block in this piece left nothing in the slot: its
+                        // entries are not read at all, stale bits may be NaN)
+                        float Ls = 0.f, wu[NW];
+#pragma unroll
+                        for (int u = 0; u < NW; ++u) {
+                            const float *gs = reinterpret_cast<const float *>(slot + C::SL_GRP + u * C::SL_GRP_BYTES);
+                            wu[u] = 0.f;
+                            if (group_in_piece(u, piece_i0, nb) && M != -INFINITY) {
+                                wu[u] = fast_exp2(gs[h] - M);
+                                Ls += wu[u] * gs[NH + h];
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < NW; ++u) {
+                            float f = 0.f;
+                            if (Ls > 0.f && wu[u] > 0.f) {
+                                const int Eu =
+                                    reinterpret_cast<const int *>(slot + C::SL_GRP + u * C::SL_GRP_BYTES)[2 * NH];
+                                f = __fdividef(wu[u] * exp2i(Eu - 6), Ls);
+                            }
+                            fac[u * NH + h] = f;
+                        }
+                        if (!whole_pair && cur.g * NH + h < a.num_q_heads)
+                            a.lse[(size_t)(2 * cta + oslot) * NH + h] =
+                                Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+                    }
+                    named_bar(BAR_WG, 128);
+                    float acc[NH];
+#pragma unroll
+                    for (int h = 0; h < NH; ++h)
+                        acc[h] = 0.f;
+#pragma unroll
+                    for (int u = 0; u < NW; ++u) {
+                        if (!group_in_piece(u, piece_i0, nb))
+                            continue;  // group-uniform
+                        uint32_t ov[NH];
+                        tmem_ld32(tmem + lane_base + C::O_COL + (uint32_t)(u * 2 + s) * NH, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < NH / 4; ++q) {
+                            const float4 f4 = reinterpret_cast<const float4 *>(fac + u * NH)[q];
+                            acc[4 * q] += f4.x * __uint_as_float(ov[4 * q]);
+                            acc[4 * q + 1] += f4.y * __uint_as_float(ov[4 * q + 1]);
+                            acc[4 * q + 2] += f4.z * __uint_as_float(ov[4 * q + 2]);
+                            acc[4 * q + 3] += f4.w * __uint_as_float(ov[4 * q + 3]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(sfree + s);  // slot s and the groups' O buffers s are free
+                    const int nh = min(NH, a.num_q_heads - cur.g * NH);  // heads of this group that exist
+                    if (whole_pair) {
+                        __nv_bfloat16 *dst = a.out + ((size_t)cur.b * a.num_q_heads + cur.g * NH) * D + tok;
+#pragma unroll
+                        for (int h = 0; h < NH; ++h)
+                            if (h < nh)
+                                dst[(size_t)h * D] = __float2bfloat16_rn(acc[h]);
+                    } else {
+                        float *dst = a.o_partial + ((size_t)(2 * cta + oslot) * NH) * D + tok;
+#pragma unroll
+                        for (int h = 0; h < NH; ++h)
+                            dst[(size_t)h * D] = acc[h];
+                    }
+                    if (!whole_pair && cur.blk == cur.nblk - 1 && wj == 0 && lane == 0) {
+                        // the pair's last piece: describe the pair for the merge kernel
+                        const long long g0 = list_first + i - cur.blk, g1 = g0 + cur.nblk - 1;
+                        const int c_lo = cta_of(g0, list_n, Ge), c_hi = cta_of(g1, list_n, Ge);
+                        int *m = a.merge_desc + (2 * cta + oslot) * 8;
+                        m[0] = cur.b;
+                        m[1] = cur.g;
+                        m[2] = c_lo;
+                        m[3] = c_hi;
+                        m[4] = (list_n * c_lo / Ge == g0) ? 0 : 1;  // slot of the pair in CTA c_lo
+                    }
+                    named_bar(BAR_WG, 128);  // fac is reused
+                }
+                // the next piece starts from empty sums (its first block sets the references)
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+                    l_acc[h] = 0.f;
+                E_run = -100;
             }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(vready + buf);
             cursor_next(cur, a, groups);
         }
-        if (*abort_flag && lane == 0 && warp == 0 && q_issued > piece + 1)
-            mbar_wait_bounded(qfull, (uint32_t)(q_issued - 1) & 1u);  // the Q copy still in flight (bounded)
-    } else if (warp == 13) {
+        // ---- teardown (workers): tid 0 reports a timeout and lets the last raw Q copy land
+        tc_fence_before();
+        bar_all();
+        if (tid == 0 && *abort_flag) {
+            set_status(a.dev_status, MQA_DEV_TIMEOUT);
+            const int qi = *q_issued;
+            if (qi > 0)
+                mbar_wait_drain(qfull, (uint32_t)(qi - 1) & 1u);
+        }
+        return;
+    } else if (warp == C::TMA_WARP) {
         // ================================================================ TMA producer
         // ring stage j % RING takes block j once O^T of block j - RING has read its V;
         // lane 4t + c fetches the block id of box c of tile t a block ahead
-        if (lane == 0) {
-            const bool p64 = a.page_size == kTileTokens;
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.k_map64 : &a.k_map))
-                         : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.v_map64 : &a.v_map))
-                         : "memory");
-        }
         Cursor pre = c0;
         int32_t idc = lane < 8 ? fetch_tile_box_id(a, pre, lane >> 2, lane & 3) : kNoBlock;
         int j = 0;
@@ -855,316 +1087,91 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             pre = nx;
         }
         if (*abort_flag && lane == 0) {
-            // let the copies still in flight land before the CTA leaves (bounded): the last
-            // block issued into each stage
+            // let the copies still in flight land before the CTA leaves: the last block
+            // issued into each stage
             for (int jj = max(0, j - RING); jj < j; ++jj)
                 for (int t = 0; t < 2; ++t)
-                    mbar_wait_bounded(tfull + 2 * (jj % RING) + t, (uint32_t)(jj / RING) & 1u);
+                    mbar_wait_drain(tfull + 2 * (jj % RING) + t, (uint32_t)(jj / RING) & 1u);
         }
-    } else if (warp == 12) {
-        // ================================================================ MMA issuer
-        if (lane == 0) {
+        tc_fence_before();
+        bar_all();
+        return;
+    } else {
+        // ================================================================ MMA issuers
+        // one issuing thread per worker group (warps MMA_WARP, then the warps after the TMA
+        // warp): S^T(i) once the group's K(i) is in tensor memory, O^T_w += V^T(i) P'(i) once its
+        // P' and V are.  Each issuer's commits track only its own MMAs, so the groups' products
+        // never queue behind one another.
+        const int w = warp == C::MMA_WARP ? 0 : warp - C::TMA_WARP;
+        if (w < NW && lane == 0) {
+            constexpr uint32_t IDESC_QK = umma_idesc_f16(128, NH, false, false);
+            constexpr uint32_t IDESC_PV = umma_idesc_f16(128, NH, true, true);
             // descriptors of the shared-memory operands at their buffers' starts
             const uint64_t qdesc0 = umma_sdesc(smem_u32(qh), C::Q_SC, C::Q_SR);
             const uint64_t vdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING), C::V_SR, C::V_SC);
-            const uint64_t pdesc0 = umma_sdesc(smem_u32(ph), C::P_SR, C::P_SC);
-            Cursor cur = c0;
-            int n_qk = 0, n_pv = 0, piece = -1, qpiece = -1;
-            uint32_t first_bits = 0;  // bit (j & 31): block j starts a piece
-            bool ok = true;
-            for (int i = 0; i < n && ok; ++i) {
-                const int buf = bufd(i);
-                const bool first = i == 0 || cur.blk == 0;
-                if (first) {
-                    first_bits |= 1u << (i & 31);
-                    ++qpiece;
-                } else {
-                    first_bits &= ~(1u << (i & 31));
-                }
-                // S^T(i) = K(i) Q^T: K from tensor memory, Q (this piece's buffer) from shared
-                // memory.  The S buffer [buf] was read by softmax(i-DEPTH), waited for before
-                // O^T(i-DEPTH) was issued.
-                if (!wait_phase(kready + buf, phd(i), abort_flag))
-                    break;
-                tc_fence_after();
-                const uint64_t qd = desc_add(qdesc0, (uint32_t)(qpiece & 1) * NH * D * 2);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_f16_ts(tmem + C::S_COL + (uint32_t)buf * NH, tmem + C::K_COL + (uint32_t)buf * 64 + 8 * kk,
-                                desc_add(qd, kk * 2 * C::Q_SC), IDESC_QK, kk > 0);
-                umma_commit(sfull + buf);
-                ++n_qk;
-                if (i >= 1)
-                    ok = issue_pv(i - 1, first_bits, piece, n_pv, tmem, vdesc0, pdesc0, pready, vready, ofree, odone,
-                                  tfree, abort_flag);
-                cursor_next(cur, a, groups);
-            }
-            if (ok && n_qk == n)
-                issue_pv(n - 1, first_bits, piece, n_pv, tmem, vdesc0, pdesc0, pready, vready, ofree, odone, tfree,
-                         abort_flag);
-            if (*abort_flag) {
-                // let the tensor core finish what was issued (bounded)
-                if (n_qk > 0)
-                    mbar_wait_bounded(sfull + bufd(n_qk - 1), phd(n_qk - 1));
-                if (n_pv > 0)
-                    mbar_wait_bounded(odone + bufd(n_pv - 1), phd(n_pv - 1));
-            }
-        }
-    } else {
-        // ================================================================ softmax
-        // thread (token tok, head half hh): warps 4-7 take heads 0-15 of their tokens,
-        // warps 8-11 heads 16-31; tensor-memory lanes by warp % 4
-        constexpr int NHH = NH / 2;
-        const int sw = warp - 4, hh = sw >> 2, tok = 32 * (warp & 3) + lane;
-        // per head: this token's sum of p.  The reference maxima (log2 domain),
-        // the same in every softmax thread, live in mref (shared memory).
-        float l_acc[NHH];
-        int E_run = -100;         // running power-of-two bound of the V scales
-        float gh = 0.f;           // log2-domain factor of the raw scores of the piece
-        int piece = -1, piece_first_i = 0;
-        bool piece_from_start = false;
-        Cursor cur = c0;
-        for (int i = 0; i < n; ++i) {
-            const int buf = bufd(i);
-            const bool first = (i == 0) || cur.blk == 0;
-            const bool last = (i == n - 1) || cur.blk == cur.nblk - 1;
-            if (first) {
-                ++piece;
-                piece_first_i = i;
-                piece_from_start = cur.blk == 0;
-                E_run = -100;
-#pragma unroll
-                for (int j = 0; j < NHH; ++j)
-                    l_acc[j] = 0.f;
-            }
-            bool ok = wait_phase(kready + buf, phd(i), abort_flag);
-            // the scales (and the piece's Q factor) are in place once K(i) is
-            const float *scb = sc + buf * 3 * BT;
-            const float ksv = scb[tok], vsv = scb[BT + tok];
-            const bool valid = scb[2 * BT + tok] != 0.f;
-            if (first)
-                gh = cred[4 + (piece & 3)];  // 4 slots: the converters run up to DEPTH blocks ahead
-            float mr[NHH];  // the reference maxima of this thread's heads, in registers while they hold
-            if (!first) {
-#pragma unroll
-                for (int q = 0; q < NHH / 4; ++q) {
-                    const float4 m4 = reinterpret_cast<const float4 *>(mref + NHH * hh)[q];
-                    mr[4 * q] = m4.x;
-                    mr[4 * q + 1] = m4.y;
-                    mr[4 * q + 2] = m4.z;
-                    mr[4 * q + 3] = m4.w;
-                }
-            }
-            ok = ok && wait_phase(sfull + buf, phd(i), abort_flag);
-            tc_fence_after();
-            uint32_t sr[NHH];
-            tmem_ld16(tmem + lane_base + C::S_COL + (uint32_t)buf * NH + NHH * hh, sr);
-            tmem_wait_ld();
-            {
-                // take the K codes' bias off the scores: kBias * sum_d Q[h][d] per head, summed in
-                // a fixed order at the piece's first block (and kept for its later blocks)
-                float bq[NHH];
-                if (first) {
-                    const float4 *qp = reinterpret_cast<const float4 *>(qpart + (piece & 3) * 4 * NH + NHH * hh);
-#pragma unroll
-                    for (int q = 0; q < NHH / 4; ++q) {
-                        const float4 p0 = qp[q], p1 = qp[NH / 4 + q], p2 = qp[NH / 2 + q], p3 = qp[3 * NH / 4 + q];
-                        bq[4 * q] = kBias * (((p0.x + p1.x) + p2.x) + p3.x);
-                        bq[4 * q + 1] = kBias * (((p0.y + p1.y) + p2.y) + p3.y);
-                        bq[4 * q + 2] = kBias * (((p0.z + p1.z) + p2.z) + p3.z);
-                        bq[4 * q + 3] = kBias * (((p0.w + p1.w) + p2.w) + p3.w);
-                    }
-                    if ((sw & 3) == 0 && lane == 0) {
-#pragma unroll
-                        for (int j = 0; j < NHH; ++j)
-                            bsum[NHH * hh + j] = bq[j];  // read from the next block on, after the barrier below
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < NHH / 4; ++q) {
-                        const float4 b4 = reinterpret_cast<const float4 *>(bsum + NHH * hh)[q];
-                        bq[4 * q] = b4.x;
-                        bq[4 * q + 1] = b4.y;
-                        bq[4 * q + 2] = b4.z;
-                        bq[4 * q + 3] = b4.w;
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < NHH; ++j)
-                    sr[j] = __float_as_uint(__uint_as_float(sr[j]) - bq[j]);
-            }
-            const float kg = ksv * gh;  // raw score -> log2 domain
-            // a piece's first block always moves the references (they start at -inf)
-            bool need = valid && (first || !(vsv <= exp2i(E_run)));
-            if (!first) {
-#pragma unroll
-                for (int j = 0; j < NHH; ++j)
-                    need |= valid && !(fmaf(__uint_as_float(sr[j]), kg, -mr[j]) <= 8.f);
-            }
-            if (named_bar_or(BAR_SM, 256, need || !ok)) {
-                if (named_bar_or(BAR_SM, 256, !ok))
-                    break;  // abort (every softmax thread leaves here together)
-                // rare: move the references to the block maxima (and the V-scale bound)
-                {
-                    float mv[NHH];
-#pragma unroll
-                    for (int j = 0; j < NHH; ++j)
-                        mv[j] = valid ? __uint_as_float(sr[j]) * kg : -INFINITY;
-                    const float wm = warp_transpose_reduce16<true>(mv, lane);  // head lane % 16's warp max
-                    if (lane < NHH)
-                        red[sw * NHH + lane] = wm;
-                }
-                float vm = valid ? vsv : 0.f;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
-                if (lane == 0)
-                    red[8 * NHH + sw] = vm;
-                named_bar(BAR_SM, 256);
-                float vmax = red[8 * NHH];
-#pragma unroll
-                for (int k = 1; k < 8; ++k)
-                    vmax = fmaxf(vmax, red[8 * NHH + k]);
-                const int E_new = max(E_run, ceil_log2_pow(vmax));
-                const int dE = E_run - E_new;
-                const float escale = dE < -126 ? 0.f : exp2i(dE);
-                // warp 4 moves the references (lane = head, over the 4 warps of its half)
-                if (sw == 0) {
-                    const int h = lane, base4 = 4 * (h >> 4) * NHH + (h & 15);
-                    const float bm = fmaxf(fmaxf(red[base4], red[base4 + NHH]),
-                                           fmaxf(red[base4 + 2 * NHH], red[base4 + 3 * NHH]));
-                    const float mo = first ? -INFINITY : mref[h];
-                    const float mn = fmaxf(mo, bm);
-                    mref[h] = mn;
-                    ofac_s[h] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
-                }
-                named_bar(BAR_SM, 256);
-#pragma unroll
-                for (int j = 0; j < NHH; ++j)
-                    l_acc[j] *= ofac_s[NHH * hh + j];
-                E_run = E_new;
-                if (!first) {
-                    // O of this piece, once O^T(i-1) has landed: row d = tok, this thread's 16 heads
-                    wait_phase(odone + bufd(i - 1), phd(i - 1), abort_flag);
+            const uint64_t pd = desc_add(umma_sdesc(smem_u32(ph), C::P_SR, C::P_SC), w * BT * NH * 2);
+            const uint32_t s_col = C::S_COL + (uint32_t)w * NH, k_col = C::K_COL + (uint32_t)w * 64;
+            Cursor c = c0;
+            int piece = -1, o_piece = -1, jw = 0, n_s = 0, n_pv = 0;
+            for (int i = 0; i < n; ++i) {
+                if (i == 0 || c.blk == 0)
+                    ++piece;
+                if (i % NW == w) {
+                    const uint32_t pj = (uint32_t)jw & 1u;
+                    // S^T(i) = K(i) Q^T: K from the group's tensor memory, Q (the piece's slot) from
+                    // shared memory; the group read its S buffer's previous contents before K(i)
+                    if (!wait_phase(kready + w, pj, abort_flag))
+                        break;
                     tc_fence_after();
-                    const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH + NHH * hh;
-                    uint32_t orr[16];
-                    tmem_ld16(tmem + lane_base + o_col, orr);
-                    tmem_wait_ld();
+                    const uint64_t qd = desc_add(qdesc0, (uint32_t)(piece & 1) * NH * D * 2);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        orr[j] = __float_as_uint(__uint_as_float(orr[j]) * (ofac_s[NHH * hh + j] * escale));
-                    tmem_st16(tmem + lane_base + o_col, orr);
-                    tmem_wait_st();
-                }
-                named_bar(BAR_SM, 256);  // reductions read before red is reused
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_f16_ts(tmem + s_col, tmem + k_col + 8 * kk, desc_add(qd, kk * 2 * C::Q_SC), IDESC_QK,
+                                    kk > 0);
+                    umma_commit(sfull + w);
+                    ++n_s;
+                    if (!wait_phase(pready + w, pj, abort_flag) || !wait_phase(vready + w, pj, abort_flag))
+                        break;
+                    // the group's first update of a piece overwrites O buffer piece & 1, last read by
+                    // the epilogue of piece - 2
+                    const bool fresh = o_piece != piece;
+                    if (fresh && piece >= 2 &&
+                        !wait_phase(sfree + (piece & 1), (uint32_t)((piece - 2) >> 1) & 1u, abort_flag))
+                        break;
+                    o_piece = piece;
+                    tc_fence_after();
+                    const uint32_t o_col = C::O_COL + (uint32_t)(w * 2 + (piece & 1)) * NH;
+                    // V: fp16 in place in ring stage i % RING; 16-token step kk = token groups 2kk,
+                    // 2kk+1 of warp kk / 2, in the K half (kk even) or the V half (kk odd)
+                    const uint64_t vd = desc_add(vdesc0, (i % RING) * C::STAGE);
 #pragma unroll
-                for (int q = 0; q < NHH / 4; ++q) {
-                    const float4 m4 = reinterpret_cast<const float4 *>(mref + NHH * hh)[q];
-                    mr[4 * q] = m4.x;
-                    mr[4 * q + 1] = m4.y;
-                    mr[4 * q + 2] = m4.z;
-                    mr[4 * q + 3] = m4.w;
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        umma_f16(tmem + o_col, desc_add(vd, (kk & 1) * C::CODES + (kk >> 1) * 4096),
+                                 desc_add(pd, kk * 2 * C::P_SR), IDESC_PV, !fresh || kk > 0);
+                    umma_commit(odone + w);
+                    umma_commit(tfree + (i % RING));  // the stage's V is read: the TMA warp may refill it
+                    ++n_pv;
+                    ++jw;
                 }
+                cursor_next(c, a, groups);
             }
-            // ---- P' = 2^(score - ref) * s_v * 2^(6-E) as fp16: row tok, heads 16hh .. 16hh+15 of P'[buf]
-            if (i >= C::DEPTH)  // P' buffer [buf] free once O^T(i-DEPTH) is done
-                wait_phase(odone + buf, phd(i - C::DEPTH), abort_flag);
-            const float vf = valid ? vsv * exp2i(6 - E_run) : 0.f;
-            uint8_t *pb = ph + buf * BT * NH * 2;
-#pragma unroll
-            for (int q = 0; q < NHH / 8; ++q) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int j0 = 8 * q + 2 * k;
-                    const float p0 = valid ? fast_exp2(fmaf(__uint_as_float(sr[j0]), kg, -mr[j0])) : 0.f;
-                    const float p1 = valid ? fast_exp2(fmaf(__uint_as_float(sr[j0 + 1]), kg, -mr[j0 + 1])) : 0.f;
-                    l_acc[j0] += p0;
-                    l_acc[j0 + 1] += p1;
-                    pk[k] = pack_half2(p0 * vf, p1 * vf);
-                }
-                *reinterpret_cast<uint4 *>(pb + core_off(tok, NHH * hh + 8 * q, C::P_SR, C::P_SC)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (*abort_flag) {
+                // let the tensor core finish what this thread issued: its last commit covers it all
+                if (n_pv > 0)
+                    mbar_wait_drain(odone + w, (uint32_t)(n_pv - 1) & 1u);
+                if (n_s > 0)
+                    mbar_wait_drain(sfull + w, (uint32_t)(n_s - 1) & 1u);
             }
-            fence_proxy_async();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(pready + buf);
-            if (last) {
-                // ---- epilogue of the piece: l per head over the 128 token rows, normalise O
-                wait_phase(odone + buf, phd(i), abort_flag);  // O^T(i) landed
-                tc_fence_after();
-                {
-                    float lv[NHH];
-#pragma unroll
-                    for (int j = 0; j < NHH; ++j)
-                        lv[j] = l_acc[j];
-                    const float ws = warp_transpose_reduce16<false>(lv, lane);  // head lane % 16's warp sum
-                    if (lane < NHH)
-                        red[sw * NHH + lane] = ws;
-                }
-                const bool whole_pair = piece_from_start && cur.blk == cur.nblk - 1;
-                const int slot = piece_first_i == 0 ? 0 : 1;
-                named_bar(BAR_SM, 256);
-                if (sw == 0) {
-                    // head lane: l, the output factor 2^(E-6) / l and (for a partial) the lse
-                    const int h = lane, base4 = 4 * (h >> 4) * NHH + (h & 15);
-                    const float l = red[base4] + red[base4 + NHH] + red[base4 + 2 * NHH] + red[base4 + 3 * NHH];
-                    ofac_s[h] = l > 0.f ? __fdividef(exp2i(E_run - 6), l) : 0.f;
-                    if (!whole_pair && cur.g * NH + h < a.num_q_heads)
-                        a.lse[(size_t)(2 * cta + slot) * NH + h] =
-                            l > 0.f ? (mref[h] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-                }
-                const uint32_t o_col = C::O_COL + (uint32_t)(piece & 1) * NH + NHH * hh;
-                uint32_t ov[NHH];
-                tmem_ld16(tmem + lane_base + o_col, ov);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(ofree + (piece & 1));
-                named_bar(BAR_SM, 256);  // ofac_s ready
-                const int nh = min(NH, a.num_q_heads - cur.g * NH);  // heads of this group that exist
-                if (whole_pair) {
-                    __nv_bfloat16 *dst = a.out + ((size_t)cur.b * a.num_q_heads + cur.g * NH + NHH * hh) * D + tok;
-#pragma unroll
-                    for (int j = 0; j < NHH; ++j)
-                        if (NHH * hh + j < nh)
-                            dst[(size_t)j * D] = __float2bfloat16_rn(__uint_as_float(ov[j]) * ofac_s[NHH * hh + j]);
-                } else {
-                    float *dst = a.o_partial + ((size_t)(2 * cta + slot) * NH + NHH * hh) * D + tok;
-#pragma unroll
-                    for (int j = 0; j < NHH; ++j)
-                        dst[(size_t)j * D] = __uint_as_float(ov[j]) * ofac_s[NHH * hh + j];
-                }
-                if (!whole_pair && cur.blk == cur.nblk - 1 && sw == 0 && lane == 0) {
-                    // the pair's last piece: describe the pair for the merge kernel
-                    const long long g0 = list_first + i - cur.blk, g1 = g0 + cur.nblk - 1;
-                    const int c_lo = cta_of(g0, list_n, Ge), c_hi = cta_of(g1, list_n, Ge);
-                    int *m = a.merge_desc + (2 * cta + slot) * 8;
-                    m[0] = cur.b;
-                    m[1] = cur.g;
-                    m[2] = c_lo;
-                    m[3] = c_hi;
-                    m[4] = (list_n * c_lo / Ge == g0) ? 0 : 1;  // slot of the pair in CTA c_lo
-                }
-                named_bar(BAR_SM, 256);  // red and ofac_s are reused by the next piece
-            }
-            cursor_next(cur, a, groups);
         }
-    }
-
-    // ---- teardown
-    tc_fence_before();
-    __syncthreads();
-    const bool aborted = *abort_flag != 0;
-    if (aborted && tid == 0)
-        set_status(a.dev_status, MQA_DEV_TIMEOUT);
-    if (warp == 12) {
-        tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        // ---- teardown (issuers and the idle warp): the workers saw every MMA complete; the
+        // MMA warp frees the tensor memory
+        tc_fence_before();
+        bar_all();
+        if (warp == C::MMA_WARP) {
+            tc_fence_after();
+            tmem_dealloc(tmem, C::TMEM_COLS);
+        }
+        return;
     }
 }
 
@@ -1176,6 +1183,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
 __global__ void __launch_bounds__(256) decode_tc_merge_kernel(const __grid_constant__ DecodeArgs a)
 {
     constexpr int NH = TcCfg::NH, D = TcCfg::D;
+    griddep_wait();
+    griddep_launch_dependents();
     const int *m = a.merge_desc + (2 * blockIdx.x) * 8;
     const int b = __ldg(m);
     if (b < 0)
@@ -1229,14 +1238,20 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s)
                                              TcCfg::SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
+        // the kernel moves registers between its warpgroups (setmaxnreg): the split must fit
+        // the registers it is launched with, or a group would wait for registers forever
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, decode_tc_kernel);
+        if (e != cudaSuccess)
+            return e;
+        if (fa.numRegs != TcCfg::REG_LAUNCH)
+            return cudaErrorInvalidConfiguration;
         attr_set.store(1, std::memory_order_release);
     }
-    decode_tc_kernel<<<a.persist_ctas, TcCfg::THREADS, TcCfg::SMEM_BYTES, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_tc_kernel, dim3(a.persist_ctas), dim3(TcCfg::THREADS), TcCfg::SMEM_BYTES, s, a);
     if (e != cudaSuccess || !a.persistent)
         return e;
-    decode_tc_merge_kernel<<<dim3(a.persist_ctas, TcCfg::NH / 8), 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_tc_merge_kernel, dim3(a.persist_ctas, TcCfg::NH / 8), dim3(256), 0, s, a);
 }
 
 int decode_tc_ctas_per_sm()

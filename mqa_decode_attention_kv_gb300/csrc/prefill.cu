@@ -64,6 +64,8 @@ template <int D>
 __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__ PrefillArgs a)
 {
     using C = PrefillCfg<D>;
+    griddep_wait();  // the append of this chunk's K/V (and q) before it on the stream
+    griddep_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *khalf = base + C::OFF_HALF;
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         if (threadIdx.x == 0) {
             set_status(a.dev_status, MQA_DEV_TIMEOUT);
             for (int j = i; j < n_tiles && j < i + C::STAGES; ++j)
-                mbar_wait_bounded(mbar + (j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u);
+                mbar_wait_drain(mbar + (j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u);
         }
         return;
     }
@@ -382,8 +384,7 @@ cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t s)
     const int QT = C::ROWS / H > 0 ? C::ROWS / H : 1;
     const int hgroups = H > C::ROWS ? H / C::ROWS : 1;
     dim3 grid((unsigned)(((a.max_q_len + QT - 1) / QT) * hgroups), (unsigned)a.batch, 1);
-    prefill_kernel<D><<<grid, 128, C::SMEM_BYTES, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prefill_kernel<D>, grid, dim3(128), C::SMEM_BYTES, s, a);
 }
 
 }  // namespace

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) quant_append_kernel(AppendArgs a)
     constexpr int kLanesPerVec = D / 8;               // 16 (d=128) or 8 (d=64)
     constexpr int kVecsPerWarp = 32 / kLanesPerVec;   // 2 or 4
     constexpr int kTokensPerWarp = kVecsPerWarp / 2;  // K and V of a token
+    griddep_wait();  // the previous kernel on the stream (which may read the slots written here) is done
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int vec = lane / kLanesPerVec;              // which vector of the warp
@@ -113,10 +115,8 @@ cudaError_t launch_quant_append(const AppendArgs &a, cudaStream_t s)
     const long long warps = ((long long)a.num_tokens + tokens_per_warp - 1) / tokens_per_warp;
     const long long blocks = (warps * 32 + threads - 1) / threads;
     if (a.head_dim == 128)
-        quant_append_kernel<128><<<(unsigned)blocks, threads, 0, s>>>(a);
-    else
-        quant_append_kernel<64><<<(unsigned)blocks, threads, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(quant_append_kernel<128>, dim3((unsigned)blocks), dim3(threads), 0, s, a);
+    return launch_pdl(quant_append_kernel<64>, dim3((unsigned)blocks), dim3(threads), 0, s, a);
 }
 
 }  // namespace mqa
