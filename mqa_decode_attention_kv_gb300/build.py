@@ -75,5 +75,35 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines: list[str], force: bool = False) -> str:
+    """Build a test-only copy of the library with extra preprocessor defines
+    (e.g. ``-DMQA_TEST_WAIT_LIMIT_NS=1``) under ``_build/<name>/``; returns its
+    path.  The product library is never affected."""
+    out = os.path.join(BUILD, name)
+    lib = os.path.join(out, "libmqa_kv.so")
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(out, exist_ok=True)
+    nvcc = _nvcc()
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(out, src.replace(".cu", ".o"))
+        r = subprocess.run([nvcc, *NVCC_FLAGS, *defines, "-c", os.path.join(CSRC, src), "-o", obj],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = lib + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp, *objs],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
