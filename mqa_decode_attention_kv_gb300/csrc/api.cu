@@ -548,6 +548,15 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
         return rc;
     if ((rc = make_code_map(&a.v_map, cache->v_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
         return rc;
+    if (D == 128 && cache->page_size == kTileTokens) {
+        // whole 64-token tiles (= pages) in one copy per tensor
+        if ((rc = make_code_map(&a.k_map64, cache->k_codes, cache->num_blocks, cache->page_size, D, kTileTokens)) !=
+            MQA_OK)
+            return rc;
+        if ((rc = make_code_map(&a.v_map64, cache->v_codes, cache->num_blocks, cache->page_size, D, kTileTokens)) !=
+            MQA_OK)
+            return rc;
+    }
     a.k_scale = cache->k_scale;
     a.v_scale = cache->v_scale;
     a.block_table = batch->block_table;

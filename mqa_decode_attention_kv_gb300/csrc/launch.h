@@ -75,7 +75,8 @@ cudaError_t launch_combine(const float *o_partial, const float *lse, int32_t bat
                            int32_t num_q_heads, int32_t head_dim, __nv_bfloat16 *out, cudaStream_t s);
 
 struct PrefillArgs {
-    CUtensorMap k_map, v_map;
+    CUtensorMap k_map, v_map;          // 16-row boxes
+    CUtensorMap k_map64, v_map64;      // 64-row boxes (tcgen05 kernel, page_size 64 only)
     const float *k_scale, *v_scale;
     const int32_t *block_table, *seq_lens, *cu_q;
     const __nv_bfloat16 *q;
@@ -86,5 +87,6 @@ struct PrefillArgs {
     float q_scale_log2;
 };
 cudaError_t launch_prefill(const PrefillArgs &a, int head_dim, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);  // head_dim 128
 
 }  // namespace mqa

@@ -1,5 +1,6 @@
 // Chunked causal prefill attention over the int8 paged cache (prefix-shared
-// blocks allowed), warp-level tensor-core version.
+// blocks allowed), warp-level tensor-core version for head_dim 64 (head_dim
+// 128 runs on the tcgen05 kernel of prefill_tc.cu).
 //
 // A CTA owns 64 query rows -- QT = 64/num_q_heads consecutive query tokens of
 // one sequence times all heads (MQA: every row reads the same K/V) -- and walks
@@ -391,7 +392,8 @@ cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t s)
 
 cudaError_t launch_prefill(const PrefillArgs &a, int head_dim, cudaStream_t s)
 {
-    return head_dim == 128 ? launch_prefill_t<128>(a, s) : launch_prefill_t<64>(a, s);
+    // head_dim 128 runs on the tcgen05 kernel (prefill_tc.cu); head_dim 64 here
+    return head_dim == 128 ? launch_prefill_tc(a, s) : launch_prefill_t<64>(a, s);
 }
 
 }  // namespace mqa

@@ -1,0 +1,633 @@
+// Chunked causal prefill attention on the 5th-generation tensor cores
+// (tcgen05), head_dim 128, over the int8 paged cache (prefix-shared blocks
+// allowed).
+//
+// A CTA owns M = 128 consecutive query rows of one sequence: 128 / H query
+// tokens times all H heads (MQA: every row reads the same K/V; the rows of
+// tokens t and heads h are contiguous in q and out).  It walks the 128-key
+// blocks its rows need, from the earliest row's window start to the last
+// row's position.  Per block j:
+//   S(j)  = Q K(j)^T     M = 128 rows, N = 128 keys, K = d: Q in tensor
+//                        memory (A), K as fp16 in shared memory (B);
+//   P'(j) = 2^(s - m) * s_v * 2^(6-E) per row and key (fp16, in tensor memory);
+//   O    += P'(j) V(j)   M = 128 rows, N = 128 d, K = keys: P' in tensor
+//                        memory (A), V as fp16 converted in place in its
+//                        ring stage (B).
+// Scores and O accumulate in fp32 tensor memory.
+//
+// Roles (16 warps, one CTA per SM):
+//   warps 0-7   softmax, two warpgroups: half hf takes keys 64 hf .. 64 hf + 63
+//               of every block, thread r of each half owns query row r
+//               (tensor-memory lane r).  Half 0 converts the row of Q to fp16
+//               times one exact power of two into tensor memory.  Per block a
+//               thread reads its 64 scores, takes off the K codes' exponent
+//               bias (kBias * sum_d Q~[r][d]), applies the K scales and the
+//               row's causal / window mask and writes P' for its keys.  The
+//               row keeps one reference maximum (moved only when a score
+//               passes it by more than 2^8; the halves agree through a
+//               barrier that ORs the need) and one power-of-two bound 2^E of
+//               the V scales.  At the end each half normalises its 64 columns
+//               of the row of O.
+//   warps 8-11  converters: thread k owns key row k of every block.  K codes
+//               to fp16 (with their exponent bias +1152) into a K buffer,
+//               V codes to fp16 in place in the ring stage, the block's K and
+//               V scales (negative K scale = key not fetched or outside the
+//               CTA's key range) and the warp's largest V scale.
+//   warp 12     lane 0 issues every tcgen05.mma and commit, S(j) one block
+//               ahead of O += P'(j-1) V(j-1); the warp owns the tensor memory.
+//   warp 13     TMA: block ids a block ahead, the codes and scales of each
+//               block into a ring stage once the O update that read the
+//               stage's previous block has completed.
+//   warps 14-15 idle (their registers go to the softmax and converter warps).
+//
+// Every wait is bounded: a wait that runs out raises a CTA abort flag, every
+// role leaves at its next check (the softmax warps all together, at the
+// barrier that ORs the flag), copies and MMAs in flight are drained, and the
+// call reports MQA_DEV_TIMEOUT.  Launched with programmatic stream
+// serialisation: every global access comes after griddep_wait().
+#include <atomic>
+#include <math.h>
+
+#include "common.cuh"
+#include "kv_stage.cuh"
+#include "launch.h"
+#include "tc.cuh"
+#include "tc_pipe.cuh"
+
+namespace mqa {
+namespace {
+
+struct PfCfg {
+    static constexpr int D = kBlockD;            // 128
+    static constexpr int M = 128;                // query rows per CTA
+    static constexpr int BK = kBlockTokens;      // keys per block
+    static constexpr int BOXES = BK / kChunkTokens;
+    static constexpr int RING = 4;
+    static constexpr int THREADS = 512;
+    static constexpr int CV_WARP0 = 8, MMA_WARP = 12, TMA_WARP = 13;
+    static constexpr int BAR_SM = 1;  // named barrier of the two softmax warpgroups
+    static constexpr int REG_LAUNCH = (65536 / THREADS) / 8 * 8;  // 128
+    static constexpr int REG_CTRL = 56;
+    static constexpr int REG_WORK = ((REG_LAUNCH * THREADS - 128 * REG_CTRL) / 384) / 8 * 8;
+    static constexpr int CODES = BK * D;
+    static constexpr int STAGE = 2 * CODES;
+    // shared memory
+    static constexpr int OFF_RING = 0;
+    static constexpr int OFF_KH = OFF_RING + RING * STAGE;        // [2] fp16 K [128 keys][128 d], core layout
+    static constexpr int OFF_SCL = OFF_KH + 2 * BK * D * 2;       // [RING][2][128] fp32 K, V token scales (TMA)
+    static constexpr int OFF_OK = OFF_SCL + RING * 2 * BK * 4;    // [RING][8] box arrived
+    static constexpr int SB_KS = 0, SB_VS = 512, SB_VMAX = 1024, SB_BYTES = 1040;
+    static constexpr int OFF_SB = OFF_OK + RING * BOXES * 4;      // [2] block scales: ks[128], vs[128], vmax[4]
+    static constexpr int OFF_XM = OFF_SB + 2 * SB_BYTES;          // [2 parity][2 halves][128] row maxima / sums
+    static constexpr int OFF_MISC = OFF_XM + 2 * 2 * M * 4;       // tmem base, abort flag
+    static constexpr int OFF_MBAR = OFF_MISC + 64;
+    static constexpr int NBAR = 3 * RING + 9;
+    static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
+    // tensor memory: Q (fp16 pairs) | O | S [2] | P' (fp16 pairs)
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t Q_COL = 0, O_COL = 64, S_COL = 192, P_COL = 448;
+    // core-matrix strides: K rows = keys (K-major B of S), V rows = keys (MN-major B of O, the
+    // same in-place layout as the decode kernel: token group warp j at 4096 j, groups 0, 1 in
+    // the K half, 2, 3 in the V half)
+    static constexpr uint32_t K_SR = 16 * 128;  // next 8 keys
+    static constexpr uint32_t K_SC = 128;       // next 8 d
+    static constexpr uint32_t V_SR = 16 * 128;  // next 8 keys (inside a 16-key MMA step)
+    static constexpr uint32_t V_SC = 128;       // next 8 d
+};
+static_assert(PfCfg::SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(PfCfg::OFF_KH % 1024 == 0 && PfCfg::STAGE % 1024 == 0, "1024-byte alignment");
+static_assert(PfCfg::OFF_SCL % 16 == 0 && PfCfg::OFF_OK % 16 == 0 && PfCfg::OFF_SB % 16 == 0 &&
+                  PfCfg::SB_BYTES % 16 == 0 && PfCfg::OFF_MISC % 16 == 0 && PfCfg::OFF_MBAR % 8 == 0,
+              "16-byte alignment");
+static_assert(PfCfg::P_COL + 64 <= PfCfg::TMEM_COLS && PfCfg::S_COL + 2 * 128 <= PfCfg::P_COL, "tensor memory");
+static_assert(128 * (3 * PfCfg::REG_WORK + PfCfg::REG_CTRL) <= PfCfg::REG_LAUNCH * PfCfg::THREADS &&
+                  PfCfg::REG_WORK >= PfCfg::REG_LAUNCH,
+              "register split within the launch allocation");
+
+constexpr float kBiasK = 1152.f;  // K codes enter the tensor core as code + 1152 (exact in fp16)
+
+// The key range of a CTA as the TMA helpers see it: blocks of two 64-token
+// tiles from tile t_first, keys [lo, L).
+struct PfPos {
+    int b, blk, t_first, lo, L;
+};
+
+__device__ __forceinline__ void pf_regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PfCfg::REG_WORK));
+}
+__device__ __forceinline__ void pf_regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfCfg::REG_CTRL));
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a)
+{
+    using C = PfCfg;
+    constexpr int D = C::D, RING = C::RING, BK = C::BK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint32_t *box_ok = reinterpret_cast<uint32_t *>(base + C::OFF_OK);
+    float *scl = reinterpret_cast<float *>(base + C::OFF_SCL);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 4);
+    uint64_t *tfull = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][2] tiles landed (TMA)
+    uint64_t *tfree = tfull + 2 * RING;  // [RING] stage free: O update of its block done (tensor core)
+    uint64_t *kvready = tfree + RING;    // [2] K fp16, V fp16 and the block's scales ready (4 converter warps)
+    uint64_t *sfull = kvready + 2;       // [2] S(j) done                                   (tensor core)
+    uint64_t *sbfree = sfull + 2;        // [2] the block's scales read                    (8 softmax warps)
+    uint64_t *pready = sbfree + 2;       // P'(j) written, S(j) read                       (8 softmax warps)
+    uint64_t *odone = pready + 1;        // O += P'(j) V(j) done                           (tensor core)
+    uint64_t *qready = odone + 1;        // Q in tensor memory                             (4 softmax warps)
+    static_assert(3 * C::RING + 9 == C::NBAR, "barrier count");
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.num_q_heads;
+    const int tpc = C::M / H;  // query tokens per CTA
+    const int b = blockIdx.y;
+    const int t_begin = blockIdx.x * tpc;
+
+    // ---- set-up (no global memory: overlaps the previous kernel)
+    if (tid == 0) {
+        for (int s = 0; s < 2 * RING; ++s)
+            mbar_init(tfull + s, 1);
+        for (int s = 0; s < RING; ++s)
+            mbar_init(tfree + s, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(kvready + s, 4);
+            mbar_init(sfull + s, 1);
+            mbar_init(sbfree + s, 8);
+        }
+        mbar_init(pready, 8);
+        mbar_init(odone, 1);
+        mbar_init(qready, 4);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::MMA_WARP)
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+    griddep_wait();
+    griddep_launch_dependents();
+
+    // ---- this CTA's rows and keys (every thread computes the same)
+    const int L = __ldg(a.seq_lens + b);
+    const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
+    const int qlen = q1 - q0;
+    const bool bad = L < 1 || L > a.max_seq_len || qlen > L || q0 < 0 || qlen < 0 || q1 > a.total_q;
+    if (bad && tid == 0 && blockIdx.x == 0)
+        set_status(a.dev_status, (L < 1 || L > a.max_seq_len) ? MQA_DEV_BAD_SEQLEN : MQA_DEV_BAD_CU);
+    const int ntok = bad ? 0 : min(qlen, t_begin + tpc) - t_begin;  // query tokens of this CTA
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (ntok <= 0) {  // uniform: nothing to compute
+        if (warp == C::MMA_WARP)
+            tmem_dealloc(tmem, C::TMEM_COLS);
+        return;
+    }
+    const int i0 = L - qlen + t_begin;     // position of the CTA's first query token
+    const int i_last = i0 + ntok - 1;      // and of its last
+    const int W = a.window;
+    const int klo = W > 0 ? max(0, i0 - W + 1) : 0;       // keys the earliest row may see
+    const int lo_max = W > 0 ? max(0, i_last - W + 1) : 0; // the window start of the latest row
+    const int t_first = klo / kTileTokens;
+    const int nb = (i_last / kTileTokens - t_first + 2) >> 1;  // 128-key blocks
+    PfPos pos0{b, 0, t_first, klo, i_last + 1};
+
+    if (warp < C::CV_WARP0 + 4)
+        pf_regs_inc();
+    else
+        pf_regs_dec();
+
+    if (warp < C::CV_WARP0) {
+        // ================================================================ softmax
+        // two warpgroups: half hf takes keys 64 hf .. 64 hf + 63 of every block for all 128
+        // rows; thread r of each half owns query row r (tensor-memory lane r).  Both halves keep
+        // the same reference per row; they agree on moving it through a barrier that ORs the
+        // need (rare), and half 0 rescales O.
+        const int hf = warp >> 2;
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int t = r / H;
+        const bool rvalid = t < ntok;
+        const int ipos = i0 + t;
+        const int lo_r = W > 0 ? max(0, ipos - W + 1) : 0;
+        const size_t qrow = ((size_t)(q0 + t_begin) * H + r) * D;
+        float* xm = reinterpret_cast<float *>(base + C::OFF_XM);  // [2 parity][2 halves][128]
+        // ---- Q row: fp16 times 2^e (exact); half 0 writes it to tensor memory.  g turns a raw
+        // score into the log2 domain, bg = kBias * sum_d Q~ * g takes the K codes' bias off
+        float g, bg;
+        {
+            uint4 qv[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                qv[c] = rvalid ? __ldg(reinterpret_cast<const uint4 *>(a.q + qrow) + c) : make_uint4(0, 0, 0, 0);
+            float mx = 0.f;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[u] << 16)), fabsf(__uint_as_float(w4[u] & 0xffff0000u))));
+            }
+            int e = 0;
+            if (mx > 0.f && isfinite(mx)) {
+                int x;
+                frexpf(mx, &x);
+                e = min(120, max(-120, 14 - x));
+            }
+            const float f = exp2i(e);
+            g = a.q_scale_log2 * exp2i(-e);
+            float qsum = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t hq[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = qv[8 * half + c];
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        hq[4 * c + u] = pack_half2(__uint_as_float(w4[u] << 16) * f, __uint_as_float(w4[u] & 0xffff0000u) * f);
+                        const __half2 h2 = *reinterpret_cast<const __half2 *>(&hq[4 * c + u]);
+                        qsum += __low2float(h2);
+                        qsum += __high2float(h2);
+                    }
+                }
+                if (hf == 0)
+                    tmem_st32(tmem + lane_base + C::Q_COL + 32 * half, hq);
+            }
+            bg = kBiasK * qsum * g;
+            if (hf == 0) {
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(qready);
+            }
+        }
+        // the row's state, the same in both halves: reference m (log2 domain), V-scale bound 2^E,
+        // and c = 6 - E - m, which turns a masked score into the exponent of p * 2^(6-E);
+        // lp: this half's sum of p * 2^(6-E)
+        float m_run = -INFINITY, cexp = 0.f, lp = 0.f;
+        int E_run = -100;
+        bool ok = true;
+        int j = 0;
+        for (; j < nb; ++j) {
+            const int b2 = j & 1;
+            ok &= wait_phase(kvready + b2, (uint32_t)(j >> 1) & 1u, abort_flag);
+            ok &= wait_phase(sfull + b2, (uint32_t)(j >> 1) & 1u, abort_flag);
+            tc_fence_after();
+            const uint8_t *sb = base + C::OFF_SB + b2 * C::SB_BYTES;
+            const float *ks = reinterpret_cast<const float *>(sb + C::SB_KS) + 64 * hf;
+            const float *vs = reinterpret_cast<const float *>(sb + C::SB_VS) + 64 * hf;
+            const int kb = (t_first + 2 * j) * kTileTokens + 64 * hf;  // first key of this half-block
+            // every row sees every key of the half-block (keys fetched permitting)
+            const bool full = kb >= lo_max && kb + 63 <= i0;
+            // ---- exponent arguments y = x + c (x the masked log2-domain score, -inf when masked)
+            float y[64];
+            float ymax = -INFINITY;
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t sr[32];
+                tmem_ld32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 64 * hf + 32 * q2, sr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 k4 = reinterpret_cast<const float4 *>(ks)[8 * q2 + c4];
+                    const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = 32 * q2 + 4 * c4 + u;
+                        const int key = kb + c;
+                        const bool v = rvalid && kv[u] >= 0.f && (full || (key >= lo_r && key <= ipos));
+                        const float yy = fmaf(fmaf(__uint_as_float(sr[4 * c4 + u]), g, -bg), kv[u], cexp);
+                        y[c] = v ? yy : -INFINITY;
+                        ymax = fmaxf(ymax, y[c]);
+                    }
+                }
+            }
+            const float vmx = fmaxf(fmaxf(reinterpret_cast<const float *>(sb + C::SB_VMAX)[0],
+                                          reinterpret_cast<const float *>(sb + C::SB_VMAX)[1]),
+                                    fmaxf(reinterpret_cast<const float *>(sb + C::SB_VMAX)[2],
+                                          reinterpret_cast<const float *>(sb + C::SB_VMAX)[3]));
+            // the reference holds while every y <= 14 - E (p <= 2^8) and the V bound covers the block;
+            // a row without a reference yet moves at its first key
+            const bool need = (m_run == -INFINITY && ymax != -INFINITY) || !(ymax <= 14.f - (float)E_run) ||
+                              !(vmx <= exp2i(E_run));
+            ok &= *abort_flag == 0;
+            if (named_bar_or(C::BAR_SM, 256, need || !ok)) {
+                if (named_bar_or(C::BAR_SM, 256, !ok))
+                    break;  // abort: both halves leave here together
+                // ---- rare: the row's reference and V bound move (both halves compute the same)
+                float *xmp = xm + b2 * 2 * C::M;
+                xmp[hf * C::M + r] = ymax - cexp;  // this half's largest masked score (log2 domain)
+                named_bar(C::BAR_SM, 256);
+                const float xmax = fmaxf(xmp[r], xmp[C::M + r]);
+                const float m_new = fmaxf(m_run, xmax);
+                const int E_new = max(E_run, ceil_log2_pow(vmx));
+                const float c_new = m_new == -INFINITY ? 0.f : (float)(6 - E_new) - m_new;
+                // old terms in the new units: 2^(m - m') 2^(E - E')
+                const float factor = m_run == -INFINITY ? 0.f : fast_exp2((m_run - m_new) + (float)(E_run - E_new));
+                lp *= factor;
+                if (hf == 0) {
+                    // O of the previous blocks (its last update done: waited here) to the new units
+                    const bool resc = j >= 1 && m_run != -INFINITY && factor != 1.f;
+                    if (__any_sync(0xffffffffu, resc)) {
+                        if (j >= 1)
+                            ok &= wait_phase(odone, (uint32_t)(j - 1) & 1u, abort_flag);
+                        tc_fence_after();
+                        const float of = resc ? factor : 1.f;
+#pragma unroll 1
+                        for (int q8 = 0; q8 < 8; ++q8) {
+                            uint32_t orr[16];
+                            tmem_ld16(tmem + lane_base + C::O_COL + 16 * q8, orr);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                orr[c] = __float_as_uint(__uint_as_float(orr[c]) * of);
+                            tmem_st16(tmem + lane_base + C::O_COL + 16 * q8, orr);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                const float dc = c_new - cexp;
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    y[c] += dc;
+                m_run = m_new;
+                E_run = E_new;
+                cexp = c_new;
+            }
+            // ---- P' = 2^y * s_v (fp16) into this half's columns, once O += P' V of the previous
+            // block has read the P' buffer
+            if (j >= 1)
+                ok &= wait_phase(odone, (uint32_t)(j - 1) & 1u, abort_flag);
+            tc_fence_after();
+            const bool live = m_run != -INFINITY;
+            uint32_t pk[32];
+            float ls = 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4) {
+                const float4 v4 = reinterpret_cast<const float4 *>(vs)[c4];
+                const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+                float p[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    p[u] = live ? fast_exp2(y[4 * c4 + u]) : 0.f;
+                    ls += p[u];
+                }
+                pk[2 * c4] = pack_half2(p[0] * vv[0], p[1] * vv[1]);
+                pk[2 * c4 + 1] = pack_half2(p[2] * vv[2], p[3] * vv[3]);
+            }
+            lp += ls;
+            tmem_st32(tmem + lane_base + C::P_COL + 32 * hf, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(sbfree + b2);
+                mbar_arrive(pready);
+            }
+        }
+        // ---- epilogue: out = O / (sum of p * 2^(6-E)), half hf writing d = 64 hf .. 64 hf + 63
+        if (j == nb) {
+            float *ls2 = xm + (nb & 1) * 2 * C::M;  // parity slot the last block did not use
+            ls2[hf * C::M + r] = lp;
+            named_bar(C::BAR_SM, 256);
+            const float lt = ls2[r] + ls2[C::M + r];
+            ok &= wait_phase(odone, (uint32_t)(nb - 1) & 1u, abort_flag);
+            tc_fence_after();
+            const float of = lt > 0.f ? 1.f / lt : 0.f;
+            uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow + 64 * hf);
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t orr[32];
+                tmem_ld32(tmem + lane_base + C::O_COL + 64 * hf + 32 * q2, orr);
+                tmem_wait_ld();
+                if (rvalid) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        dst[4 * q2 + c] = make_uint4(
+                            pack_bf16x2(__uint_as_float(orr[8 * c + 0]) * of, __uint_as_float(orr[8 * c + 1]) * of),
+                            pack_bf16x2(__uint_as_float(orr[8 * c + 2]) * of, __uint_as_float(orr[8 * c + 3]) * of),
+                            pack_bf16x2(__uint_as_float(orr[8 * c + 4]) * of, __uint_as_float(orr[8 * c + 5]) * of),
+                            pack_bf16x2(__uint_as_float(orr[8 * c + 6]) * of, __uint_as_float(orr[8 * c + 7]) * of));
+                }
+            }
+        }
+        tc_fence_before();
+        bar_all();
+        if (tid == 0 && *abort_flag)
+            set_status(a.dev_status, MQA_DEV_TIMEOUT);
+        return;
+    } else if (warp < C::CV_WARP0 + 4) {
+        // ================================================================ converters
+        const int wj = warp - C::CV_WARP0;
+        const int kr = 32 * wj + lane;  // key row of every block
+        uint8_t *kh0 = base + C::OFF_KH;
+        bool ok = true;
+        for (int j = 0; j < nb; ++j) {
+            const int r = j % RING, b2 = j & 1;
+            uint8_t *st = base + C::OFF_RING + r * C::STAGE;
+            ok &= wait_phase(tfull + 2 * r + (wj >> 1), (uint32_t)(j / RING) & 1u, abort_flag);
+            if (j >= 2) {
+                // K buffer b2 was read by S(j-2); the scales of slot b2 by the softmax of block j-2
+                ok &= wait_phase(sfull + b2, (uint32_t)((j - 2) >> 1) & 1u, abort_flag);
+                ok &= wait_phase(sbfree + b2, (uint32_t)((j - 2) >> 1) & 1u, abort_flag);
+            }
+            if (__any_sync(0xffffffffu, !ok))
+                break;
+            const uint8_t *crow = st + kr * D;
+            // ---- K: 128 codes -> fp16 (+1152) into K buffer b2, row kr
+            uint8_t *kh = kh0 + b2 * BK * D * 2;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint4 kc[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    kc[jj] = *reinterpret_cast<const uint4 *>(crow + ((uint32_t)((4 * half + jj) ^ (kr & 7)) << 4));
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    uint32_t h8[8];
+                    const uint4 kv = kc[jj];
+                    const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t tt = w4[u] ^ 0x80808080u;
+                        h8[2 * u] = __byte_perm(tt, 0x64646464u, 0x5140);
+                        h8[2 * u + 1] = __byte_perm(tt, 0x64646464u, 0x7362);
+                    }
+                    const int dch = 16 * (4 * half + jj);  // d of the chunk
+                    *reinterpret_cast<uint4 *>(kh + core_off(kr, dch, C::K_SR, C::K_SC)) =
+                        make_uint4(h8[0], h8[1], h8[2], h8[3]);
+                    *reinterpret_cast<uint4 *>(kh + core_off(kr, dch + 8, C::K_SR, C::K_SC)) =
+                        make_uint4(h8[4], h8[5], h8[6], h8[7]);
+                }
+            }
+            // ---- V: fp16 in place over this warp's 8 KB of codes (its own key rows)
+            uint4 vc[D / 16];
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c)
+                vc[c] = *reinterpret_cast<const uint4 *>(crow + C::CODES + ((uint32_t)(c ^ (kr & 7)) << 4));
+            __syncwarp();
+            {
+                const int gq = lane >> 3;
+                uint8_t *vb = st + (gq >> 1) * C::CODES + wj * 4096 + (gq & 1) * 2048 + (lane & 7) * 16;
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t v8[8];
+                    i8x4_to_f16x2x2(vc[c].x, v8[0], v8[1]);
+                    i8x4_to_f16x2x2(vc[c].y, v8[2], v8[3]);
+                    i8x4_to_f16x2x2(vc[c].z, v8[4], v8[5]);
+                    i8x4_to_f16x2x2(vc[c].w, v8[6], v8[7]);
+                    *reinterpret_cast<uint4 *>(vb + (2 * c) * C::V_SC) = make_uint4(v8[0], v8[1], v8[2], v8[3]);
+                    *reinterpret_cast<uint4 *>(vb + (2 * c + 1) * C::V_SC) = make_uint4(v8[4], v8[5], v8[6], v8[7]);
+                }
+            }
+            // ---- the block's scales: a negative K scale marks a key not fetched or outside the range
+            {
+                const int key = (t_first + 2 * j) * kTileTokens + kr;
+                const bool fetched = box_ok[r * C::BOXES + (kr >> 4)] != 0;
+                const bool valid = fetched && key >= klo && key <= i_last;
+                uint8_t *sb = base + C::OFF_SB + b2 * C::SB_BYTES;
+                const float ksv = scl[r * 2 * BK + kr], vsv = scl[r * 2 * BK + BK + kr];
+                reinterpret_cast<float *>(sb + C::SB_KS)[kr] = valid ? ksv : -1.f;
+                reinterpret_cast<float *>(sb + C::SB_VS)[kr] = valid ? vsv : 0.f;
+                float vm = valid ? vsv : 0.f;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                if (lane == 0)
+                    reinterpret_cast<float *>(sb + C::SB_VMAX)[wj] = vm;
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(kvready + b2);
+        }
+        tc_fence_before();
+        bar_all();
+        return;
+    } else if (warp == C::TMA_WARP) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            const bool p64 = a.page_size == kTileTokens;
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.k_map64 : &a.k_map))
+                         : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.v_map64 : &a.v_map))
+                         : "memory");
+        }
+        PfPos pre = pos0;
+        int32_t idc = lane < 8 ? fetch_tile_box_id(a, pre, lane >> 2, lane & 3) : kNoBlock;
+        int j = 0;
+        for (; j < nb; ++j) {
+            const int r = j % RING;
+            if (j >= RING &&
+                !__all_sync(0xffffffffu, wait_phase(tfree + r, (uint32_t)(j / RING - 1) & 1u, abort_flag)))
+                break;
+            PfPos nx = pre;
+            ++nx.blk;
+            const int32_t id_next = (lane < 8 && j + 1 < nb) ? fetch_tile_box_id(a, nx, lane >> 2, lane & 3) : kNoBlock;
+            issue_block(a, pre, lane, idc, base + C::OFF_RING + r * C::STAGE, scl + r * 2 * BK, tfull + 2 * r,
+                        box_ok + r * C::BOXES);
+            idc = id_next;
+            pre = nx;
+        }
+        if (*abort_flag && lane == 0) {
+            // the copies still in flight land before the CTA leaves
+            for (int jj = max(0, j - RING); jj < j; ++jj)
+                for (int t = 0; t < 2; ++t)
+                    mbar_wait_drain(tfull + 2 * (jj % RING) + t, (uint32_t)(jj / RING) & 1u);
+        }
+        tc_fence_before();
+        bar_all();
+        return;
+    } else {
+        // ================================================================ MMA issuer (and idle warps)
+        if (warp == C::MMA_WARP && lane == 0) {
+            constexpr uint32_t IDESC_S = umma_idesc_f16(128, BK, false, false);
+            constexpr uint32_t IDESC_O = umma_idesc_f16(128, D, false, true);
+            const uint64_t kdesc0 = umma_sdesc(smem_u32(base + C::OFF_KH), C::K_SC, C::K_SR);
+            const uint64_t vdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING), C::V_SR, C::V_SC);
+            int n_s = 0, n_o = 0;
+            // O += P'(k) V(k): P' from tensor memory, V (fp16 in place in ring stage k % RING) from
+            // shared memory; 16-key step kk = key groups 2kk, 2kk+1 of converter warp kk / 2
+            auto issue_o = [&](int k) -> bool {
+                if (!wait_phase(pready, (uint32_t)k & 1u, abort_flag))
+                    return false;
+                tc_fence_after();
+                const uint64_t vd = desc_add(vdesc0, (k % RING) * C::STAGE);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    umma_f16_ts(tmem + C::O_COL, tmem + C::P_COL + 8 * kk,
+                                desc_add(vd, (kk & 1) * C::CODES + (kk >> 1) * 4096), IDESC_O, k > 0 || kk > 0);
+                umma_commit(odone);
+                umma_commit(tfree + (k % RING));  // the stage's V is read: the TMA warp may refill it
+                ++n_o;
+                return true;
+            };
+            bool ok = wait_phase(qready, 0u, abort_flag);
+            for (int j = 0; j < nb && ok; ++j) {
+                const int b2 = j & 1;
+                // S(j) = Q K(j)^T into S buffer b2 (read by the softmax of block j-2, whose P' the
+                // O update issued last step waited for)
+                if (!wait_phase(kvready + b2, (uint32_t)(j >> 1) & 1u, abort_flag))
+                    break;
+                tc_fence_after();
+                const uint64_t kd = desc_add(kdesc0, (uint32_t)b2 * BK * D * 2);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_f16_ts(tmem + C::S_COL + (uint32_t)b2 * BK, tmem + C::Q_COL + 8 * kk,
+                                desc_add(kd, kk * 2 * C::K_SC), IDESC_S, kk > 0);
+                umma_commit(sfull + b2);
+                ++n_s;
+                if (j >= 1)
+                    ok = issue_o(j - 1);
+            }
+            if (ok && n_s == nb)
+                issue_o(nb - 1);
+            if (*abort_flag) {
+                if (n_o > 0)
+                    mbar_wait_drain(odone, (uint32_t)(n_o - 1) & 1u);
+                if (n_s > 0)
+                    mbar_wait_drain(sfull + ((n_s - 1) & 1), (uint32_t)((n_s - 1) >> 1) & 1u);
+            }
+        }
+        tc_fence_before();
+        bar_all();
+        if (warp == C::MMA_WARP) {
+            tc_fence_after();
+            tmem_dealloc(tmem, C::TMEM_COLS);
+        }
+        return;
+    }
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s)
+{
+    static std::atomic<int> attr_set{0};
+    if (!attr_set.load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             PfCfg::SMEM_BYTES);
+        if (e != cudaSuccess)
+            return e;
+        // the kernel moves registers between its warpgroups (setmaxnreg): the split must fit the
+        // registers it is launched with, or a group would wait for registers forever
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
+        if (e != cudaSuccess)
+            return e;
+        if (fa.numRegs != PfCfg::REG_LAUNCH)
+            return cudaErrorInvalidConfiguration;
+        attr_set.store(1, std::memory_order_release);
+    }
+    const int tpc = PfCfg::M / a.num_q_heads;
+    dim3 grid((unsigned)((a.max_q_len + tpc - 1) / tpc), (unsigned)a.batch, 1);
+    return launch_pdl(prefill_tc_kernel, grid, dim3(PfCfg::THREADS), PfCfg::SMEM_BYTES, s, a);
+}
+
+}  // namespace mqa

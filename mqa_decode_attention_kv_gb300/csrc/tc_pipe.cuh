@@ -1,0 +1,155 @@
+// Pipeline helpers shared by the tcgen05 kernels (decode and prefill): bounded
+// mbarrier waits with a CTA abort flag, named barriers, tensor-core issue from
+// tensor memory, descriptor arithmetic.
+#pragma once
+
+#include "common.cuh"
+#include "kv_stage.cuh"
+#include "tc.cuh"
+
+namespace mqa {
+
+// Bounded wait that also gives up once another role has raised the abort
+// flag; a wait that runs out raises it.  Returns false when giving up.
+__device__ __forceinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag);
+
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    return mbar_try_wait(bar, parity) || wait_phase_slow(bar, parity, abort_flag);
+}
+
+// The polling loop (inlined: a called function could not serve warpgroups that
+// run with different register counts).
+__device__ __forceinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity))
+                return true;
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void named_bar(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Barrier over n threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// A: tensor memory, B: shared memory descriptor.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred pa;\n\tsetp.ne.u32 pa, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
+}
+
+// Shared-memory descriptor plus a byte offset (the address field counts 16 B).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The CTA-wide barrier of the teardown.  Every role ends with its own copy of
+// the teardown (the roles run with different register counts and never rejoin).
+__device__ __forceinline__ void bar_all() { asm volatile("bar.sync 0;" ::: "memory"); }
+
+// Key blocks of the tcgen05 kernels: 128 tokens (two 64-token tiles) of head_dim 128.
+constexpr int kBlockTokens = 128, kBlockD = 128;
+
+// Cache row of the first token of box c of tile T in block `id`, or -1 when
+// the box is not fetched (kNoBlock, or an id outside the pool: reported).
+template <class Args>
+__device__ __forceinline__ int box_row(const Args &a, int32_t id, int T, int c)
+{
+    const bool ok = id >= 0 && id < a.num_blocks;
+    if (!ok && id != kNoBlock)
+        set_status(a.dev_status, MQA_DEV_BAD_BLOCK);
+    return ok ? id * a.page_size + (T * kTileTokens + c * kChunkTokens) % a.page_size : -1;
+}
+
+// Block id of box c (16 tokens) of tile t (64 tokens, 0 or 1) of the block at
+// position p (fields b, blk, t_first, lo, L); kNoBlock when the box lies outside [lo, L).
+template <class Args, class Pos>
+__device__ __forceinline__ int32_t fetch_tile_box_id(const Args &a, const Pos &p, int t, int c)
+{
+    const int T = p.t_first + 2 * p.blk + t;
+    return T <= (p.L - 1) / kTileTokens
+               ? fetch_box_block(a.block_table + (size_t)p.b * a.max_blocks, a.page_size, T, c, p.lo, p.L)
+               : kNoBlock;
+}
+
+// Both tiles of the block at p into ring stage `stage`, their token scales into
+// `scl` ([2][128] fp32: K, V), issued by the TMA warp (every lane calls; lane
+// 4t + c holds the id of box c of tile t).  A tile inside [lo, L) on one
+// 64-token page goes as one 64-row copy per tensor (and one 256-byte copy per
+// scale row), any other tile as its 16-row boxes that overlap [lo, L) (and
+// 64-byte scale copies).  One arrival per tile on bars[t] with its byte count;
+// box_ok[4t + c] records whether box c comes.
+template <class Args, class Pos>
+__device__ __forceinline__ void issue_block(const Args &a, const Pos &p, int lane, int32_t idc, uint8_t *stage,
+                                            float *scl, uint64_t *bars, uint32_t *oks)
+{
+    constexpr int D = kBlockD, CODES = kBlockTokens * kBlockD, BT = kBlockTokens;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int T = p.t_first + 2 * p.blk + t;
+        const int c = lane - 4 * t;
+        const bool mine = c >= 0 && c < 4;
+        const int row = mine ? box_row(a, idc, T, c) : -1;
+        const uint32_t okmask = (__ballot_sync(0xffffffffu, row >= 0) >> (4 * t)) & 0xfu;
+        const int row0 = __shfl_sync(0xffffffffu, row, 4 * t);
+        const bool whole = a.page_size == kTileTokens && okmask == 0xfu && T * kTileTokens >= p.lo &&
+                           T * kTileTokens + kTileTokens <= p.L;
+        if (mine)
+            oks[4 * t + c] = row >= 0 ? 1u : 0u;
+        __syncwarp();  // the flags are written before the arrival (a tile with nothing to fetch completes on it)
+        if (lane == 0)
+            mbar_arrive_expect_tx(bars + t, 2u * (uint32_t)__popc(okmask) * kChunkTokens * (D + 4));
+        __syncwarp();
+        if (whole) {
+            if (lane == 0) {
+                tma_load_2d(stage + t * kTileTokens * D, &a.k_map64, 0, row0, bars + t);
+                tma_load_2d(stage + CODES + t * kTileTokens * D, &a.v_map64, 0, row0, bars + t);
+                bulk_load(scl + t * kTileTokens, a.k_scale + row0, kTileTokens * 4, bars + t);
+                bulk_load(scl + BT + t * kTileTokens, a.v_scale + row0, kTileTokens * 4, bars + t);
+            }
+        } else if (row >= 0) {
+            const int box = 4 * t + c;
+            tma_load_2d(stage + box * kChunkTokens * D, &a.k_map, 0, row, bars + t);
+            tma_load_2d(stage + CODES + box * kChunkTokens * D, &a.v_map, 0, row, bars + t);
+            bulk_load(scl + box * kChunkTokens, a.k_scale + row, kChunkTokens * 4, bars + t);
+            bulk_load(scl + BT + box * kChunkTokens, a.v_scale + row, kChunkTokens * 4, bars + t);
+        }
+    }
+}
+
+}  // namespace mqa

@@ -60,7 +60,7 @@ def run(st, window, rows=None):
     return got, ref
 
 
-@pytest.mark.parametrize("heads,d,page", [(32, 128, 64), (8, 64, 16), (16, 128, 16), (64, 128, 64)])
+@pytest.mark.parametrize("heads,d,page", [(32, 128, 64), (8, 64, 16), (16, 128, 16), (64, 128, 64), (8, 128, 64)])
 def test_prefill_prefix_shared_ragged(heads, d, page):
     rng = np.random.default_rng(heads + d + page)
     counts = [100, 37, 64, 1, 129, 65]
