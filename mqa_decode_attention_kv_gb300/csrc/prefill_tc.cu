@@ -9,7 +9,8 @@
 // row's position.  Per block j:
 //   S(j)  = Q K(j)^T     M = 128 rows, N = 128 keys, K = d: Q in tensor
 //                        memory (A), K as fp16 in shared memory (B);
-//   P'(j) = 2^(s - m) * s_v * 2^(6-E) per row and key (fp16, in tensor memory);
+//   P'(j) = 2^(s - m) * s_v * 2^(6-E) per row and key (fp16, in tensor memory
+//                        in place of S(j));
 //   O    += P'(j) V(j)   M = 128 rows, N = 128 d, K = keys: P' in tensor
 //                        memory (A), V as fp16 converted in place in its
 //                        ring stage (B).
@@ -76,16 +77,17 @@ struct PfCfg {
     static constexpr int OFF_KH = OFF_RING + RING * STAGE;        // [2] fp16 K [128 keys][128 d], core layout
     static constexpr int OFF_SCL = OFF_KH + 2 * BK * D * 2;       // [RING][2][128] fp32 K, V token scales (TMA)
     static constexpr int OFF_OK = OFF_SCL + RING * 2 * BK * 4;    // [RING][8] box arrived
-    static constexpr int SB_KS = 0, SB_VS = 512, SB_VMAX = 1024, SB_BYTES = 1040;
-    static constexpr int OFF_SB = OFF_OK + RING * BOXES * 4;      // [2] block scales: ks[128], vs[128], vmax[4]
+    static constexpr int SB_KS = 0, SB_VS = 512, SB_VMAX = 1024, SB_ALL = 1040, SB_BYTES = 1056;
+    static constexpr int OFF_SB = OFF_OK + RING * BOXES * 4;      // [2] ks[128], vs[128], vmax[4], all-valid[4]
     static constexpr int OFF_XM = OFF_SB + 2 * SB_BYTES;          // [2 parity][2 halves][128] row maxima / sums
     static constexpr int OFF_MISC = OFF_XM + 2 * 2 * M * 4;       // tmem base, abort flag
     static constexpr int OFF_MBAR = OFF_MISC + 64;
     static constexpr int NBAR = 3 * RING + 9;
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
-    // tensor memory: Q (fp16 pairs) | O | S [2] | P' (fp16 pairs)
+    // tensor memory: Q (fp16 pairs) | O | S [2]; P'(j) (fp16 pairs) replaces S(j) in its own
+    // buffer once read: keys 0-63 at columns 0-31 of the buffer, keys 64-127 at 64-95
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t Q_COL = 0, O_COL = 64, S_COL = 192, P_COL = 448;
+    static constexpr uint32_t Q_COL = 0, O_COL = 64, S_COL = 192;
     // core-matrix strides: K rows = keys (K-major B of S), V rows = keys (MN-major B of O, the
     // same in-place layout as the decode kernel: token group warp j at 4096 j, groups 0, 1 in
     // the K half, 2, 3 in the V half)
@@ -99,12 +101,48 @@ static_assert(PfCfg::OFF_KH % 1024 == 0 && PfCfg::STAGE % 1024 == 0, "1024-byte 
 static_assert(PfCfg::OFF_SCL % 16 == 0 && PfCfg::OFF_OK % 16 == 0 && PfCfg::OFF_SB % 16 == 0 &&
                   PfCfg::SB_BYTES % 16 == 0 && PfCfg::OFF_MISC % 16 == 0 && PfCfg::OFF_MBAR % 8 == 0,
               "16-byte alignment");
-static_assert(PfCfg::P_COL + 64 <= PfCfg::TMEM_COLS && PfCfg::S_COL + 2 * 128 <= PfCfg::P_COL, "tensor memory");
+static_assert(PfCfg::S_COL + 2 * 128 <= PfCfg::TMEM_COLS, "tensor memory");
 static_assert(128 * (3 * PfCfg::REG_WORK + PfCfg::REG_CTRL) <= PfCfg::REG_LAUNCH * PfCfg::THREADS &&
                   PfCfg::REG_WORK >= PfCfg::REG_LAUNCH,
               "register split within the launch allocation");
 
 constexpr float kBiasK = 1152.f;  // K codes enter the tensor core as code + 1152 (exact in fp16)
+
+// Packed fp32 pairs (one instruction for two lanes of arithmetic) and a 3-input maximum.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 // The key range of a CTA as the TMA helpers see it: blocks of two 64-token
 // tiles from tile t_first, keys [lo, L).
@@ -285,31 +323,50 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             const float *ks = reinterpret_cast<const float *>(sb + C::SB_KS) + 64 * hf;
             const float *vs = reinterpret_cast<const float *>(sb + C::SB_VS) + 64 * hf;
             const int kb = (t_first + 2 * j) * kTileTokens + 64 * hf;  // first key of this half-block
-            // every row sees every key of the half-block (keys fetched permitting)
-            const bool full = kb >= lo_max && kb + 63 <= i0;
-            // ---- exponent arguments y = x + c (x the masked log2-domain score, -inf when masked)
-            float y[64];
-            float ymax = -INFINITY;
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t sr[32];
-                tmem_ld32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 64 * hf + 32 * q2, sr);
+            // every row sees every key of the half-block, and every key was fetched
+            const int *allv = reinterpret_cast<const int *>(sb + C::SB_ALL);
+            const bool full = kb >= lo_max && kb + 63 <= i0 && allv[2 * hf] != 0 && allv[2 * hf + 1] != 0 && rvalid;
+            // ---- exponent arguments y = x + c (x the masked log2-domain score, -inf when masked),
+            // as fp32 pairs: y = ((S g - b g) k_s) + c
+            uint64_t y2[32];
+            float ymx[2] = {-INFINITY, -INFINITY};  // independent partial maxima
+            {
+                uint32_t sr2[2][32];
+                tmem_ld32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 64 * hf, sr2[0]);
+                tmem_ld32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 64 * hf + 32, sr2[1]);
                 tmem_wait_ld();
+                const uint64_t g2 = f2pack(g, g), nbg2 = f2pack(-bg, -bg), c2 = f2pack(cexp, cexp);
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    const float4 k4 = reinterpret_cast<const float4 *>(ks)[8 * q2 + c4];
-                    const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+                for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int c = 32 * q2 + 4 * c4 + u;
-                        const int key = kb + c;
-                        const bool v = rvalid && kv[u] >= 0.f && (full || (key >= lo_r && key <= ipos));
-                        const float yy = fmaf(fmaf(__uint_as_float(sr[4 * c4 + u]), g, -bg), kv[u], cexp);
-                        y[c] = v ? yy : -INFINITY;
-                        ymax = fmaxf(ymax, y[c]);
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 k4 = reinterpret_cast<const float4 *>(ks)[8 * q2 + c4];
+                        const uint32_t *sv = &sr2[q2][4 * c4];
+                        const int c = 32 * q2 + 4 * c4;  // first key (of the half-block) of the four
+                        uint64_t ya = fma2(fma2(f2pack(__uint_as_float(sv[0]), __uint_as_float(sv[1])), g2, nbg2),
+                                           f2pack(k4.x, k4.y), c2);
+                        uint64_t yb = fma2(fma2(f2pack(__uint_as_float(sv[2]), __uint_as_float(sv[3])), g2, nbg2),
+                                           f2pack(k4.z, k4.w), c2);
+                        float y0, y1, y2v, y3;
+                        f2unpack(ya, y0, y1);
+                        f2unpack(yb, y2v, y3);
+                        if (!full) {
+                            const int key = kb + c;
+                            y0 = (rvalid && k4.x >= 0.f && key >= lo_r && key <= ipos) ? y0 : -INFINITY;
+                            y1 = (rvalid && k4.y >= 0.f && key + 1 >= lo_r && key + 1 <= ipos) ? y1 : -INFINITY;
+                            y2v = (rvalid && k4.z >= 0.f && key + 2 >= lo_r && key + 2 <= ipos) ? y2v : -INFINITY;
+                            y3 = (rvalid && k4.w >= 0.f && key + 3 >= lo_r && key + 3 <= ipos) ? y3 : -INFINITY;
+                            ya = f2pack(y0, y1);
+                            yb = f2pack(y2v, y3);
+                        }
+                        y2[c / 2] = ya;
+                        y2[c / 2 + 1] = yb;
+                        ymx[0] = max3f(ymx[0], y0, y1);
+                        ymx[1] = max3f(ymx[1], y2v, y3);
                     }
                 }
             }
+            const float ymax = fmaxf(ymx[0], ymx[1]);
             const float vmx = fmaxf(fmaxf(reinterpret_cast<const float *>(sb + C::SB_VMAX)[0],
                                           reinterpret_cast<const float *>(sb + C::SB_VMAX)[1]),
                                     fmaxf(reinterpret_cast<const float *>(sb + C::SB_VMAX)[2],
@@ -354,37 +411,40 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
                         tmem_wait_st();
                     }
                 }
-                const float dc = c_new - cexp;
+                const uint64_t dc2 = f2pack(c_new - cexp, c_new - cexp);
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    y[c] += dc;
+                for (int c = 0; c < 32; ++c)
+                    y2[c] = add2(y2[c], dc2);
                 m_run = m_new;
                 E_run = E_new;
                 cexp = c_new;
             }
-            // ---- P' = 2^y * s_v (fp16) into this half's columns, once O += P' V of the previous
-            // block has read the P' buffer
-            if (j >= 1)
-                ok &= wait_phase(odone, (uint32_t)(j - 1) & 1u, abort_flag);
-            tc_fence_after();
+            // ---- P' = 2^y * s_v (fp16) in place of this half's scores in S buffer b2 (the O update
+            // that read this buffer's previous P' was issued before S(j), which it holds now)
             const bool live = m_run != -INFINITY;
             uint32_t pk[32];
-            float ls = 0.f;
+            uint64_t ls2 = 0;  // (0.f, 0.f): independent partial sums
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
                 const float4 v4 = reinterpret_cast<const float4 *>(vs)[c4];
-                const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-                float p[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    p[u] = live ? fast_exp2(y[4 * c4 + u]) : 0.f;
-                    ls += p[u];
-                }
-                pk[2 * c4] = pack_half2(p[0] * vv[0], p[1] * vv[1]);
-                pk[2 * c4 + 1] = pack_half2(p[2] * vv[2], p[3] * vv[3]);
+                float y0, y1, y2v, y3;
+                f2unpack(y2[2 * c4], y0, y1);
+                f2unpack(y2[2 * c4 + 1], y2v, y3);
+                const uint64_t pa = live ? f2pack(fast_exp2(y0), fast_exp2(y1)) : 0ull;
+                const uint64_t pb = live ? f2pack(fast_exp2(y2v), fast_exp2(y3)) : 0ull;
+                ls2 = add2(ls2, add2(pa, pb));
+                float q0, q1, q2v, q3;
+                f2unpack(mul2(pa, f2pack(v4.x, v4.y)), q0, q1);
+                f2unpack(mul2(pb, f2pack(v4.z, v4.w)), q2v, q3);
+                pk[2 * c4] = pack_half2(q0, q1);
+                pk[2 * c4 + 1] = pack_half2(q2v, q3);
             }
-            lp += ls;
-            tmem_st32(tmem + lane_base + C::P_COL + 32 * hf, pk);
+            {
+                float la, lb;
+                f2unpack(ls2, la, lb);
+                lp += la + lb;
+            }
+            tmem_st32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 64 * hf, pk);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -501,8 +561,11 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1)
                     vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
-                if (lane == 0)
+                const bool allv = __all_sync(0xffffffffu, valid);
+                if (lane == 0) {
                     reinterpret_cast<float *>(sb + C::SB_VMAX)[wj] = vm;
+                    reinterpret_cast<int *>(sb + C::SB_ALL)[wj] = allv ? 1 : 0;
+                }
             }
             fence_proxy_async();
             __syncwarp();
@@ -554,16 +617,18 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             const uint64_t kdesc0 = umma_sdesc(smem_u32(base + C::OFF_KH), C::K_SC, C::K_SR);
             const uint64_t vdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING), C::V_SR, C::V_SC);
             int n_s = 0, n_o = 0;
-            // O += P'(k) V(k): P' from tensor memory, V (fp16 in place in ring stage k % RING) from
-            // shared memory; 16-key step kk = key groups 2kk, 2kk+1 of converter warp kk / 2
+            // O += P'(k) V(k): P' from S buffer k & 1 (keys 16kk .. 16kk+15 at column
+            // 64 (kk / 4) + 8 (kk % 4)), V (fp16 in place in ring stage k % RING) from shared memory;
+            // 16-key step kk = key groups 2kk, 2kk+1 of converter warp kk / 2
             auto issue_o = [&](int k) -> bool {
                 if (!wait_phase(pready, (uint32_t)k & 1u, abort_flag))
                     return false;
                 tc_fence_after();
                 const uint64_t vd = desc_add(vdesc0, (k % RING) * C::STAGE);
+                const uint32_t pcol = C::S_COL + (uint32_t)(k & 1) * BK;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_f16_ts(tmem + C::O_COL, tmem + C::P_COL + 8 * kk,
+                    umma_f16_ts(tmem + C::O_COL, tmem + pcol + 64 * (kk >> 2) + 8 * (kk & 3),
                                 desc_add(vd, (kk & 1) * C::CODES + (kk >> 1) * 4096), IDESC_O, k > 0 || kk > 0);
                 umma_commit(odone);
                 umma_commit(tfree + (k % RING));  // the stage's V is read: the TMA warp may refill it
@@ -573,8 +638,8 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             bool ok = wait_phase(qready, 0u, abort_flag);
             for (int j = 0; j < nb && ok; ++j) {
                 const int b2 = j & 1;
-                // S(j) = Q K(j)^T into S buffer b2 (read by the softmax of block j-2, whose P' the
-                // O update issued last step waited for)
+                // S(j) = Q K(j)^T into S buffer b2: its last contents, P'(j-2), were read by the O
+                // update issued in the previous step (the tensor core runs this thread's MMAs in order)
                 if (!wait_phase(kvready + b2, (uint32_t)(j >> 1) & 1u, abort_flag))
                     break;
                 tc_fence_after();
