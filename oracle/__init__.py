@@ -45,11 +45,11 @@ def _load():
             i32 = ctypes.c_int32
             lib.oracle_quantize_token.argtypes = [P, i32, P, P]
             lib.oracle_quantize_token.restype = None
-            lib.oracle_quant_append.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, i32, P, P, P]
+            lib.oracle_quant_append.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, i32, P, P, P, i32]
             lib.oracle_quant_append.restype = i32
             lib.oracle_attention.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, i32, i32,
                                              P, i32, P, P, i32, ctypes.c_double, i32, i32,
-                                             P, P, P, ctypes.c_int64, P]
+                                             P, P, P, ctypes.c_int64, P, i32]
             lib.oracle_attention.restype = i32
             lib.oracle_combine.argtypes = [P, P, i32, ctypes.c_int64, i32, P, P]
             lib.oracle_combine.restype = None
@@ -107,9 +107,11 @@ def quantize_tokens(x_bits: np.ndarray):
 
 
 def quant_append(cache: Cache, block_table: np.ndarray, seq_lens: np.ndarray,
-                 cu_new: np.ndarray, k_new: np.ndarray, v_new: np.ndarray) -> None:
+                 cu_new: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, ring_blocks: int = 0) -> None:
     """Quantise ``k_new``/``v_new`` (bf16 bits ``[T, d]``) and store them at the
-    last ``cu_new[b+1]-cu_new[b]`` positions of each sequence, in place."""
+    last ``cu_new[b+1]-cu_new[b]`` positions of each sequence, in place.  With
+    ``ring_blocks = R > 0`` page ``p // page_size`` lives in table entry
+    ``(p // page_size) % R`` (a window-bounded cache keeping R pages)."""
     lib = _load()
     bt = np.ascontiguousarray(block_table, np.int32)
     sl = np.ascontiguousarray(seq_lens, np.int32)
@@ -119,17 +121,19 @@ def quant_append(cache: Cache, block_table: np.ndarray, seq_lens: np.ndarray,
     rc = lib.oracle_quant_append(_p(cache.k_codes), _p(cache.v_codes), _p(cache.k_scale),
                                  _p(cache.v_scale), cache.num_blocks, cache.page_size,
                                  cache.head_dim, _p(bt), bt.shape[1], _p(sl), sl.shape[0],
-                                 _p(cu), _p(k), _p(v))
+                                 _p(cu), _p(k), _p(v), int(ring_blocks))
     if rc != 0:
         raise ValueError("oracle_quant_append: index out of range")
 
 
 def attention(cache: Cache, block_table: np.ndarray, seq_lens: np.ndarray, q: np.ndarray,
               row_seq: np.ndarray, row_pos: np.ndarray, window: int, sm_scale: float,
-              key_range: tuple[int, int] | None = None, want_probs: bool = False):
+              key_range: tuple[int, int] | None = None, want_probs: bool = False, ring_blocks: int = 0):
     """Exact attention of query rows ``q`` (bf16 bits ``[rows, H, d]``).
     Returns ``(out fp64 [rows,H,d], lse fp64 [rows,H])`` and, with ``want_probs``,
-    the weights ``fp64 [rows, H, max_len]`` (zero outside each row's key set)."""
+    the weights ``fp64 [rows, H, max_len]`` (zero outside each row's key set).
+    ``ring_blocks``: as for ``quant_append``; a key whose page is not among the
+    sequence's R most recent raises ValueError."""
     lib = _load()
     q = np.ascontiguousarray(q, np.uint16)
     rows, H, d = q.shape
@@ -153,21 +157,21 @@ def attention(cache: Cache, block_table: np.ndarray, seq_lens: np.ndarray, q: np
                               _p(bt), bt.shape[1], _p(sl), sl.shape[0], H, _p(q), rows,
                               _p(rs), _p(rp), int(window), float(sm_scale), int(kb), int(ke),
                               _p(out), _p(lse), _p(probs) if probs is not None else None,
-                              stride, _p(scratch))
+                              stride, _p(scratch), int(ring_blocks))
     if rc != 0:
         raise ValueError("oracle_attention: index out of range")
     return (out, lse, probs) if want_probs else (out, lse)
 
 
 def decode(cache: Cache, block_table, seq_lens, q, window: int, sm_scale: float,
-           seqs: np.ndarray | None = None):
+           seqs: np.ndarray | None = None, ring_blocks: int = 0):
     """Decode: the query of sequence b (``q[b]``, bf16 bits ``[B, H, d]``) sits at
     position ``seq_lens[b]-1``.  ``seqs`` restricts to a subset of sequences."""
     sl = np.asarray(seq_lens, np.int32)
     seqs = np.arange(sl.shape[0]) if seqs is None else np.asarray(seqs)
     qq = np.ascontiguousarray(np.asarray(q)[seqs])
     return attention(cache, block_table, sl, qq, seqs.astype(np.int32),
-                     (sl[seqs] - 1).astype(np.int32), window, sm_scale)
+                     (sl[seqs] - 1).astype(np.int32), window, sm_scale, ring_blocks=ring_blocks)
 
 
 def prefill_rows(cu_q: np.ndarray, seq_lens: np.ndarray):

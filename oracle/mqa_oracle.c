@@ -18,6 +18,12 @@
  *    sequence b lives in physical block block_table[b][p / page] at row
  *    p % page -- a pure re-addressing (LLM-inference workshop transcript,
  *    01:01:35-01:03:22, PagedAttention: logical blocks mapped to physical ones).
+ *    A window-bounded cache (ring_blocks = R > 0) keeps only the R most recent
+ *    pages of a sequence: page p / page lives in table entry (p / page) % R,
+ *    and a later page overwrites the entry of the page R before it (the local
+ *    layers of the "Character.AI inference article", secret 1, attend over a
+ *    1024-token window only, so older keys need not stay resident).  A key
+ *    is resident iff its page is one of the R most recent of the sequence.
  *  - attention (oracle_attention): multi-query attention -- every query head
  *    attends to the one shared K/V head ("Character.AI inference article",
  *    secret 1, "use MQA everywhere"; workshop 00:44:39-00:45:08).  A local layer
@@ -88,16 +94,22 @@ int oracle_quant_append(int8_t *k_codes, int8_t *v_codes, float *k_scale, float 
                         int32_t num_blocks, int32_t page_size, int32_t d,
                         const int32_t *block_table, int32_t max_blocks,
                         const int32_t *seq_lens, int32_t batch, const int32_t *cu_new,
-                        const uint16_t *k_new, const uint16_t *v_new)
+                        const uint16_t *k_new, const uint16_t *v_new, int32_t ring_blocks)
 {
+    if (ring_blocks < 0 || ring_blocks > max_blocks)
+        return ORACLE_EINVAL;
     for (int32_t b = 0; b < batch; ++b) {
         int32_t n = cu_new[b + 1] - cu_new[b];
         int32_t first = seq_lens[b] - n;
         if (n < 0 || first < 0)
             return ORACLE_EINVAL;
+        if (ring_blocks > 0 && (int64_t)n > (int64_t)ring_blocks * page_size)
+            return ORACLE_EINVAL; /* the call's own tokens would overwrite one another */
         for (int32_t t = 0; t < n; ++t) {
             int32_t pos = first + t;
             int32_t lb = pos / page_size;
+            if (ring_blocks > 0)
+                lb %= ring_blocks;
             if (lb >= max_blocks)
                 return ORACLE_EINVAL;
             int32_t blk = block_table[(int64_t)b * max_blocks + lb];
@@ -141,9 +153,11 @@ int oracle_attention(const int8_t *k_codes, const int8_t *v_codes,
                      const int32_t *row_pos, int32_t window, double sm_scale,
                      int32_t key_begin, int32_t key_end,
                      double *out, double *lse, double *probs, int64_t probs_stride,
-                     double *scratch)
+                     double *scratch, int32_t ring_blocks)
 {
     const int32_t H = num_q_heads;
+    if (ring_blocks < 0 || ring_blocks > max_blocks)
+        return ORACLE_EINVAL;
     for (int32_t r = 0; r < rows; ++r) {
         const int32_t b = row_seq[r];
         const int32_t i = row_pos[r];
@@ -176,7 +190,13 @@ int oracle_attention(const int8_t *k_codes, const int8_t *v_codes,
         /* scores s_j = sm_scale * <q_h, k^_j> */
         for (int32_t jj = 0; jj < n; ++jj) {
             const int32_t j = lo + jj;
-            const int32_t lb = j / page_size;
+            int32_t lb = j / page_size;
+            if (ring_blocks > 0) {
+                /* resident only among the sequence's ring_blocks most recent pages */
+                if (lb <= (seq_lens[b] - 1) / page_size - ring_blocks)
+                    return ORACLE_EINVAL;
+                lb %= ring_blocks;
+            }
             if (lb >= max_blocks)
                 return ORACLE_EINVAL;
             const int32_t blk = block_table[(int64_t)b * max_blocks + lb];
@@ -213,7 +233,8 @@ int oracle_attention(const int8_t *k_codes, const int8_t *v_codes,
         /* out_h = sum_j p_hj v^_j */
         for (int32_t jj = 0; jj < n; ++jj) {
             const int32_t j = lo + jj;
-            const int32_t blk = block_table[(int64_t)b * max_blocks + j / page_size];
+            const int32_t lb = ring_blocks > 0 ? (j / page_size) % ring_blocks : j / page_size;
+            const int32_t blk = block_table[(int64_t)b * max_blocks + lb];
             const int64_t slot = (int64_t)blk * page_size + j % page_size;
             dequant_row(v_codes + slot * d, v_scale[slot], d, kh);
             for (int32_t h = 0; h < H; ++h) {
