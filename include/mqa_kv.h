@@ -72,7 +72,8 @@ typedef struct mqa_kv_cache {
     int32_t head_dim;
 } mqa_kv_cache;
 
-/* A ragged batch over paged caches (shared by all caches of a layer stack).
+/* A ragged batch over paged caches (shared by all caches that use the same
+ * block table).
  *   block_table: int32 [batch][max_blocks]; entry i of sequence b is the
  *                physical block of its tokens [i*page, (i+1)*page).
  *   seq_lens:    int32 [batch]; tokens in the cache INCLUDING the ones the
@@ -80,7 +81,22 @@ typedef struct mqa_kv_cache {
  *   seq_lens_host: optional host copy of seq_lens (NULL allowed).  When given it
  *                is validated on the host and used to plan split-KV work.
  *   max_seq_len: host; an upper bound of every seq_lens entry, at most
- *                max_blocks * page_size. */
+ *                max_blocks * page_size unless ring_blocks > 0.
+ *   ring_blocks: host; 0 = the table maps every page of a sequence.  R > 0 = a
+ *                window-bounded cache for local layers: each sequence keeps only
+ *                its R most recent pages, page i living in table entry i % R
+ *                (a newer page overwrites the entry of the page R before it),
+ *                R <= max_blocks.  Local layers of the "Character.AI inference
+ *                article" (secret 1) attend over a 1024-token window, so their
+ *                caches need ceil(1024 / page) + 1 pages per sequence, not the
+ *                whole history.  Calls that read such a cache must stay inside
+ *                the resident pages: mqa_decode_attn needs window > 0 and
+ *                R >= (window - 1) / page + 2; mqa_prefill_attn needs window > 0
+ *                and R >= (window + max_q_len - 2) / page + 2 (its chunk's keys
+ *                and the windows of all its queries); otherwise
+ *                MQA_ERR_INVALID_ARG.  kv_quant_append flags MQA_DEV_BAD_CU and
+ *                skips a sequence appending more than R * page tokens in one
+ *                call (they would overwrite one another). */
 typedef struct mqa_batch {
     const int32_t *block_table;
     const int32_t *seq_lens;
@@ -88,6 +104,7 @@ typedef struct mqa_batch {
     int32_t batch;
     int32_t max_blocks;
     int32_t max_seq_len;
+    int32_t ring_blocks;
 } mqa_batch;
 
 /* Quantise and append new K/V tokens (one int8 code per element plus one fp32

@@ -49,7 +49,8 @@ class _Cache(ctypes.Structure):
 class _Batch(ctypes.Structure):
     _fields_ = [("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
                 ("seq_lens_host", ctypes.c_void_p), ("batch", ctypes.c_int32),
-                ("max_blocks", ctypes.c_int32), ("max_seq_len", ctypes.c_int32)]
+                ("max_blocks", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("ring_blocks", ctypes.c_int32)]
 
 
 _lib_handle = None
@@ -154,16 +155,18 @@ class Batch:
     seq_lens: "object"           # torch.int32 [batch] (device)
     seq_lens_host: np.ndarray | None
     max_seq_len: int
+    ring_blocks: int = 0         # > 0: window-bounded cache, page i in table entry i % ring_blocks
 
     @classmethod
     def from_host(cls, block_table: np.ndarray, seq_lens: np.ndarray, device="cuda",
-                  with_host_lens: bool = True, max_seq_len: int | None = None) -> "Batch":
+                  with_host_lens: bool = True, max_seq_len: int | None = None,
+                  ring_blocks: int = 0) -> "Batch":
         import torch
         bt = torch.from_numpy(np.ascontiguousarray(block_table, np.int32)).to(device)
         sl_np = np.ascontiguousarray(seq_lens, np.int32)
         sl = torch.from_numpy(sl_np).to(device)
         mx = int(sl_np.max()) if max_seq_len is None else int(max_seq_len)
-        return cls(bt, sl, sl_np.copy() if with_host_lens else None, mx)
+        return cls(bt, sl, sl_np.copy() if with_host_lens else None, mx, int(ring_blocks))
 
     @property
     def batch(self) -> int:
@@ -175,7 +178,7 @@ class Batch:
             self._host_keep = np.ascontiguousarray(self.seq_lens_host, np.int32)
             host = self._host_keep.ctypes.data
         return _Batch(_ptr(self.block_table), _ptr(self.seq_lens), host, self.batch,
-                      int(self.block_table.shape[1]), int(self.max_seq_len))
+                      int(self.block_table.shape[1]), int(self.max_seq_len), int(self.ring_blocks))
 
 
 def _caches_array(caches: Sequence[KVCache]):

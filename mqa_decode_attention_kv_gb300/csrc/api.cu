@@ -46,7 +46,10 @@ int check_batch(const mqa_batch *bt, int page_size)
         return MQA_OK;
     if (bt->block_table == nullptr || bt->seq_lens == nullptr || bt->max_blocks < 1 || bt->max_seq_len < 1)
         return MQA_ERR_INVALID_ARG;
-    if ((int64_t)bt->max_seq_len > (int64_t)bt->max_blocks * page_size)
+    if (bt->ring_blocks < 0 || bt->ring_blocks > bt->max_blocks)
+        return MQA_ERR_INVALID_ARG;
+    // a full table maps every page; a ring keeps only the most recent ones
+    if (bt->ring_blocks == 0 && (int64_t)bt->max_seq_len > (int64_t)bt->max_blocks * page_size)
         return MQA_ERR_INVALID_ARG;
     if (bt->seq_lens_host != nullptr)
         for (int b = 0; b < bt->batch; ++b)
@@ -295,6 +298,18 @@ size_t counters_offset(int32_t batch, int32_t heads, int32_t head_dim, int32_t s
 
 int head_groups(int32_t heads) { return (heads + 31) / 32; }
 
+// A window-bounded cache (ring of R pages) serves only reads inside its resident
+// pages: the R most recent pages of a sequence hold any run of up to
+// (R - 1) * page keys that ends at its last token, i.e. R >= (keys - 1) / page + 2.
+bool ring_covers(const mqa_batch *bt, int32_t window, int32_t extra_keys, int page_size)
+{
+    if (bt->ring_blocks == 0)
+        return true;
+    if (window <= 0)
+        return false;
+    return (int64_t)bt->ring_blocks >= ((int64_t)window + extra_keys - 1) / page_size + 2;
+}
+
 }  // namespace
 
 extern "C" {
@@ -347,6 +362,7 @@ int kv_quant_append(const mqa_kv_cache *cache, const mqa_batch *batch, const int
     a.cu_new = cu_new;
     a.batch = batch->batch;
     a.max_blocks = batch->max_blocks;
+    a.ring = batch->ring_blocks;
     a.num_tokens = num_new_tokens;
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
@@ -403,6 +419,8 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
     rc = check_batch(batch, cache->page_size);
     if (rc != MQA_OK)
         return rc;
+    if (!ring_covers(batch, window, 0, cache->page_size))
+        return MQA_ERR_INVALID_ARG;
     if (batch->batch == 0)
         return MQA_OK;
     if (q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out))
@@ -482,6 +500,7 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
     a.num_blocks = cache->num_blocks;
     a.page_size = cache->page_size;
     a.max_seq_len = batch->max_seq_len;
+    a.ring = batch->ring_blocks;
     a.num_q_heads = num_q_heads;
     a.window = window;
     a.tiles_per_split = plan.tiles_per_split;
@@ -539,6 +558,8 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
         return MQA_OK;
     if (max_q_len < 1 || max_q_len > batch->max_seq_len)
         return MQA_ERR_INVALID_ARG;
+    if (!ring_covers(batch, window, max_q_len - 1, cache->page_size))
+        return MQA_ERR_INVALID_ARG;
     if (cu_q == nullptr || q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out))
         return MQA_ERR_INVALID_ARG;
     const int D = cache->head_dim;
@@ -570,6 +591,7 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
     a.num_blocks = cache->num_blocks;
     a.page_size = cache->page_size;
     a.max_seq_len = batch->max_seq_len;
+    a.ring = batch->ring_blocks;
     a.num_q_heads = num_q_heads;
     a.window = window;
     a.total_q = total_q;

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(128, 3) decode_kernel(const __grid_constant__ 
         for (int i = 0; i < n_tiles && i < S; ++i) {
             issued[i * kChunksPerTile + warp] = i;
             issue_kv_box<D>(a.k_map, a.v_map, a.k_scale, a.v_scale,
-                            fetch_box_block(table, a.page_size, tb + i, warp, lo, L), a.num_blocks, a.page_size,
+                            fetch_box_block(table, a.page_size, tb + i, warp, lo, L, a.ring), a.num_blocks, a.page_size,
                             a.dev_status, base + C::OFF_CODES + i * C::STAGE_CODES,
                             reinterpret_cast<float *>(base + C::OFF_SCALES) + i * 2 * kTileTokens,
                             mbar + i * kChunksPerTile + warp, box_ok + i * kChunksPerTile + warp, tb + i, warp);
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(128, 3) decode_kernel(const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < BPW; ++j)
             id_pf[j] = (lane == 0 && i + S < n_tiles)
-                           ? fetch_box_block(table, a.page_size, T + S, tg * BPW + j, lo, L) : kNoBlock;
+                           ? fetch_box_block(table, a.page_size, T + S, tg * BPW + j, lo, L, a.ring) : kNoBlock;
         bool okj[BPW];
 #pragma unroll
         for (int j = 0; j < BPW; ++j) {

@@ -32,13 +32,16 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t col)
 // Physical block ids of the four 16-token boxes of tile T (tokens [64T, 64T+64)):
 // kNoBlock for a box outside the key range [lo, L).  The loads are independent, so a
 // caller can issue them a tile ahead of use.
+// With ring > 0 (a window-bounded cache) page p lives in table entry p % ring.
+__device__ __forceinline__ int table_entry(int page, int ring) { return ring > 0 ? page % ring : page; }
+
 __device__ __forceinline__ void fetch_tile_blocks(const int32_t *table, int page_size, int T, int lo, int L,
-                                                  int32_t (&ids)[kChunksPerTile])
+                                                  int ring, int32_t (&ids)[kChunksPerTile])
 {
 #pragma unroll
     for (int c = 0; c < kChunksPerTile; ++c) {
         const int t0 = T * kTileTokens + c * kChunkTokens;
-        ids[c] = (t0 + kChunkTokens > lo && t0 < L) ? __ldg(table + t0 / page_size) : kNoBlock;
+        ids[c] = (t0 + kChunkTokens > lo && t0 < L) ? __ldg(table + table_entry(t0 / page_size, ring)) : kNoBlock;
     }
 }
 
@@ -102,10 +105,10 @@ __device__ __forceinline__ void issue_kv_tile(const CUtensorMap &k_map, const CU
                                               const float *k_scale, const float *v_scale, const int32_t *table,
                                               int num_blocks, int page_size, int32_t *dev_status,
                                               uint8_t *codes_dst, float *scales_dst, uint64_t *bar,
-                                              uint32_t *stage_mask, int T, int lo, int L)
+                                              uint32_t *stage_mask, int T, int lo, int L, int ring)
 {
     int32_t ids[kChunksPerTile];
-    fetch_tile_blocks(table, page_size, T, lo, L, ids);
+    fetch_tile_blocks(table, page_size, T, lo, L, ring, ids);
     issue_kv_tile_ids<D>(k_map, v_map, k_scale, v_scale, ids, num_blocks, page_size, dev_status, codes_dst,
                          scales_dst, bar, stage_mask, T);
 }
@@ -140,10 +143,11 @@ __device__ __forceinline__ void issue_kv_box(const CUtensorMap &k_map, const CUt
 }
 
 // Block id of box c of tile T (kNoBlock when the box lies outside [lo, L)).
-__device__ __forceinline__ int32_t fetch_box_block(const int32_t *table, int page_size, int T, int c, int lo, int L)
+__device__ __forceinline__ int32_t fetch_box_block(const int32_t *table, int page_size, int T, int c, int lo, int L,
+                                                   int ring)
 {
     const int t0 = T * kTileTokens + c * kChunkTokens;
-    return (t0 + kChunkTokens > lo && t0 < L) ? __ldg(table + t0 / page_size) : kNoBlock;
+    return (t0 + kChunkTokens > lo && t0 < L) ? __ldg(table + table_entry(t0 / page_size, ring)) : kNoBlock;
 }
 
 }  // namespace mqa

@@ -35,6 +35,7 @@ struct AppendArgs {
     int32_t num_blocks, page_size, head_dim;
     const int32_t *block_table, *seq_lens, *cu_new;
     int32_t batch, max_blocks;
+    int32_t ring;                      // > 0: window-bounded cache, page p in table entry p % ring
     int32_t num_tokens;
     const __nv_bfloat16 *k_new, *v_new;
     int32_t *dev_status;
@@ -52,6 +53,7 @@ struct DecodeArgs {
     int32_t *counters;                 // [batch][head groups] zeroed tickets: fused merge, or null
     int32_t *dev_status;
     int32_t batch, max_blocks, num_blocks, page_size, max_seq_len;
+    int32_t ring;                      // > 0: window-bounded cache, page p in table entry p % ring
     int32_t num_q_heads, window;
     int32_t tiles_per_split, num_splits;
     float q_scale_log2;                // sm_scale * log2(e)
@@ -83,6 +85,7 @@ struct PrefillArgs {
     __nv_bfloat16 *out;
     int32_t *dev_status;
     int32_t batch, max_blocks, num_blocks, page_size, max_seq_len;
+    int32_t ring;                      // > 0: window-bounded cache, page p in table entry p % ring
     int32_t num_q_heads, window, total_q, max_q_len;
     float q_scale_log2;
 };

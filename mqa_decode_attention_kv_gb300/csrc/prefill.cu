@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
             issue_kv_tile<D>(a.k_map, a.v_map, a.k_scale, a.v_scale, a.block_table + (size_t)b * a.max_blocks,
                              a.num_blocks, a.page_size, a.dev_status, base + C::OFF_CODES + i * KvStage<D>::CODE_PAIR,
                              reinterpret_cast<float *>(base + C::OFF_SCALES) + i * 2 * kTileTokens, mbar + i,
-                             stage_mask + i, tb + i, klo, Lkeys);
+                             stage_mask + i, tb + i, klo, Lkeys, a.ring);
     }
 
     // ---- this thread's two rows (g and g+8 of the warp's 16)
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
                              a.num_blocks, a.page_size, a.dev_status,
                              base + C::OFF_CODES + stage * KvStage<D>::CODE_PAIR,
                              reinterpret_cast<float *>(base + C::OFF_SCALES) + stage * 2 * kTileTokens, mbar + stage,
-                             stage_mask + stage, tb + i + C::STAGES, klo, Lkeys);
+                             stage_mask + stage, tb + i + C::STAGES, klo, Lkeys, a.ring);
 
         // ---- S = Q K^T (16 rows x 64 keys per warp)
         float s[8][4];

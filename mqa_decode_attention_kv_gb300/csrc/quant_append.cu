@@ -6,6 +6,7 @@
 // each lane writes 8 codes (8 bytes).  Bit-exact with IEEE fp32 division and
 // round-half-even conversion (no fast-math anywhere in this file).
 #include "common.cuh"
+#include "kv_stage.cuh"
 #include "launch.h"
 
 namespace mqa {
@@ -69,12 +70,13 @@ __global__ void __launch_bounds__(256) quant_append_kernel(AppendArgs a)
     const int32_t c0 = __ldg(a.cu_new + b), c1 = __ldg(a.cu_new + b + 1);
     const int32_t L = __ldg(a.seq_lens + b);
     const int32_t pos = L - (c1 - c0) + (token - c0);
-    if (pos < 0 || pos >= L || c1 < c0) {
+    // a window-bounded cache holds ring pages: more new tokens than that would overwrite one another
+    if (pos < 0 || pos >= L || c1 < c0 || (a.ring > 0 && c1 - c0 > a.ring * a.page_size)) {
         if (sub == 0)
             set_status(a.dev_status, MQA_DEV_BAD_CU);
         return;
     }
-    const int32_t lb = pos / a.page_size;
+    const int32_t lb = table_entry(pos / a.page_size, a.ring);
     if (lb >= a.max_blocks) {
         if (sub == 0)
             set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);

@@ -103,7 +103,7 @@ __device__ __forceinline__ int32_t fetch_tile_box_id(const Args &a, const Pos &p
 {
     const int T = p.t_first + 2 * p.blk + t;
     return T <= (p.L - 1) / kTileTokens
-               ? fetch_box_block(a.block_table + (size_t)p.b * a.max_blocks, a.page_size, T, c, p.lo, p.L)
+               ? fetch_box_block(a.block_table + (size_t)p.b * a.max_blocks, a.page_size, T, c, p.lo, p.L, a.ring)
                : kNoBlock;
 }
 

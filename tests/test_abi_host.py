@@ -154,3 +154,37 @@ def test_auto_splits_validation(L):
     b, keep = batch(lens=[10, 20])
     assert L.mqa_decode_auto_splits(ctypes.byref(b), 0, 8, 96, 16) == mk.MQA_ERR_UNSUPPORTED
     assert L.mqa_decode_auto_splits(ctypes.byref(b), -5, 8, 64, 16) == mk.MQA_ERR_INVALID_ARG
+
+
+def test_ring_argument_validation(L):
+    """Window-bounded caches (ring_blocks = R > 0): R within the table, a
+    window on every read, and enough resident pages for that window."""
+    c = cache(page=16)
+    # R outside [0, max_blocks]
+    b, k = batch(lens=[10, 20], ring_blocks=-1)
+    assert decode(L, c, b, window=16) == mk.MQA_ERR_INVALID_ARG
+    b, k = batch(lens=[10, 20], ring_blocks=5)
+    assert decode(L, c, b, window=16) == mk.MQA_ERR_INVALID_ARG
+    # a ring may serve sequences longer than its table (4 entries x 16 tokens)
+    be, _ = batch(n=0, max_seq_len=10000, ring_blocks=4)
+    assert decode(L, c, be, window=48) == mk.MQA_OK              # (48 - 1) / 16 + 2 = 4 pages
+    assert decode(L, c, be, window=49) == mk.MQA_ERR_INVALID_ARG  # needs 5
+    assert decode(L, c, be, window=0) == mk.MQA_ERR_INVALID_ARG   # global attention reads evicted pages
+    # ... but a full table may not
+    bf, kf = batch(lens=[10, 20], max_seq_len=10000)
+    assert decode(L, c, bf, window=48) == mk.MQA_ERR_INVALID_ARG
+    # prefill: the chunk's keys and the windows of all its queries must be resident
+    arr = (mk._Cache * 1)(c)
+    lm = (ctypes.c_int32 * 1)(0)
+
+    def prefill(b, window, max_q):
+        return L.mqa_prefill_attn(arr, 1, lm, 1, 0, window, ctypes.byref(b), FAKE, 10, max_q, FAKE, FAKE, 8,
+                                  0.125, None, None)
+    br, kr = batch(lens=[100, 90], max_seq_len=100, ring_blocks=4)
+    assert prefill(br, 16, 34) == mk.MQA_ERR_INVALID_ARG   # (16 + 34 - 2) / 16 + 2 = 5 pages > 4
+    assert prefill(br, 49, 1) == mk.MQA_ERR_INVALID_ARG    # (49 + 1 - 2) / 16 + 2 = 5 pages > 4
+    assert prefill(br, 0, 1) == mk.MQA_ERR_INVALID_ARG     # global attention reads evicted pages
+    # append accepts the ring (its per-sequence chunk bound is checked on the device)
+    b, k = batch(lens=[10, 20], ring_blocks=5)
+    assert L.kv_quant_append(ctypes.byref(c), ctypes.byref(b), FAKE, 3, FAKE, FAKE, None, None) \
+        == mk.MQA_ERR_INVALID_ARG
