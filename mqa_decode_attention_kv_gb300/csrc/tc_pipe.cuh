@@ -108,46 +108,59 @@ __device__ __forceinline__ int32_t fetch_tile_box_id(const Args &a, const Pos &p
 }
 
 // Both tiles of the block at p into ring stage `stage`, their token scales into
-// `scl` ([2][128] fp32: K, V), issued by the TMA warp (every lane calls; lane
-// 4t + c holds the id of box c of tile t).  A tile inside [lo, L) on one
-// 64-token page goes as one 64-row copy per tensor (and one 256-byte copy per
-// scale row), any other tile as its 16-row boxes that overlap [lo, L) (and
-// 64-byte scale copies).  One arrival per tile on bars[t] with its byte count;
-// box_ok[4t + c] records whether box c comes.
+// `scl` ([2][128] fp32: K, V).  Lane 4t + c holds the id of box c of tile t.
+// A tile inside [lo, L) on one 64-token page goes as one 64-row copy per tensor
+// (and one 256-byte copy per scale row), any other tile as its 16-row boxes
+// that overlap [lo, L) (and 64-byte scale copies).  `part` 0 issues the K codes
+// and scales, 1 the V ones, -1 both: two warps may share a block (one part
+// each), each arriving once per tile on bars[t] with its byte count; the part-0
+// (or only) warp records in oks[4t + c] whether box c comes.  The copies are
+// spread over the lanes: one copy instruction takes a thread a few hundred
+// cycles to issue, and the lanes' and warps' issues overlap.
 template <class Args, class Pos>
 __device__ __forceinline__ void issue_block(const Args &a, const Pos &p, int lane, int32_t idc, uint8_t *stage,
-                                            float *scl, uint64_t *bars, uint32_t *oks)
+                                            float *scl, uint64_t *bars, uint32_t *oks, int part = -1)
 {
     constexpr int D = kBlockD, CODES = kBlockTokens * kBlockD, BT = kBlockTokens;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int T = p.t_first + 2 * p.blk + t;
-        const int c = lane - 4 * t;
-        const bool mine = c >= 0 && c < 4;
-        const int row = mine ? box_row(a, idc, T, c) : -1;
-        const uint32_t okmask = (__ballot_sync(0xffffffffu, row >= 0) >> (4 * t)) & 0xfu;
-        const int row0 = __shfl_sync(0xffffffffu, row, 4 * t);
-        const bool whole = a.page_size == kTileTokens && okmask == 0xfu && T * kTileTokens >= p.lo &&
-                           T * kTileTokens + kTileTokens <= p.L;
-        if (mine)
-            oks[4 * t + c] = row >= 0 ? 1u : 0u;
-        __syncwarp();  // the flags are written before the arrival (a tile with nothing to fetch completes on it)
-        if (lane == 0)
-            mbar_arrive_expect_tx(bars + t, 2u * (uint32_t)__popc(okmask) * kChunkTokens * (D + 4));
-        __syncwarp();
-        if (whole) {
-            if (lane == 0) {
-                tma_load_2d(stage + t * kTileTokens * D, &a.k_map64, 0, row0, bars + t);
-                tma_load_2d(stage + CODES + t * kTileTokens * D, &a.v_map64, 0, row0, bars + t);
-                bulk_load(scl + t * kTileTokens, a.k_scale + row0, kTileTokens * 4, bars + t);
-                bulk_load(scl + BT + t * kTileTokens, a.v_scale + row0, kTileTokens * 4, bars + t);
-            }
-        } else if (row >= 0) {
-            const int box = 4 * t + c;
-            tma_load_2d(stage + box * kChunkTokens * D, &a.k_map, 0, row, bars + t);
-            tma_load_2d(stage + CODES + box * kChunkTokens * D, &a.v_map, 0, row, bars + t);
-            bulk_load(scl + box * kChunkTokens, a.k_scale + row, kChunkTokens * 4, bars + t);
-            bulk_load(scl + BT + box * kChunkTokens, a.v_scale + row, kChunkTokens * 4, bars + t);
+    const int tb = lane >> 2, c = lane & 3;  // lanes 0-7: tile tb, box c
+    const int Tb = p.t_first + 2 * p.blk + (tb & 1);
+    const int row = lane < 8 ? box_row(a, idc, Tb, c) : -1;
+    const uint32_t okall = __ballot_sync(0xffffffffu, row >= 0);
+    // per tile t: whole_t, and row_t = the cache row of its first token (both tiles in
+    // registers; a lane picks its tile's with a select, never an indexed array)
+    const int row_0 = __shfl_sync(0xffffffffu, row, 0), row_1 = __shfl_sync(0xffffffffu, row, 4);
+    const int T0 = p.t_first + 2 * p.blk;
+    const bool p64 = a.page_size == kTileTokens;
+    const bool whole_0 = p64 && (okall & 0xfu) == 0xfu && T0 * kTileTokens >= p.lo && (T0 + 1) * kTileTokens <= p.L;
+    const bool whole_1 =
+        p64 && ((okall >> 4) & 0xfu) == 0xfu && (T0 + 1) * kTileTokens >= p.lo && (T0 + 2) * kTileTokens <= p.L;
+    if (lane < 8 && part <= 0)
+        oks[lane] = row >= 0 ? 1u : 0u;
+    __syncwarp();  // the flags are written before the arrival (a tile with nothing to fetch completes on it)
+    if (lane < 2) {
+        const uint32_t per_part = (uint32_t)__popc((okall >> (4 * lane)) & 0xfu) * kChunkTokens * (D + 4);
+        mbar_arrive_expect_tx(bars + lane, part < 0 ? 2u * per_part : per_part);
+    }
+    __syncwarp();
+    const int p_lo = part < 0 ? 0 : part, p_hi = part < 0 ? 1 : part;
+    // whole tiles: lane 8 + 4t + 2q + k issues part q's codes (k = 0) or scales (k = 1) of tile t
+    if (lane >= 8 && lane < 16) {
+        const int t = (lane - 8) >> 2, q = ((lane - 8) >> 1) & 1, k = lane & 1;
+        const int r0 = t ? row_1 : row_0;
+        if ((t ? whole_1 : whole_0) && q >= p_lo && q <= p_hi) {
+            if (k == 0)
+                tma_load_2d(stage + q * CODES + t * kTileTokens * D, q ? &a.v_map64 : &a.k_map64, 0, r0, bars + t);
+            else
+                bulk_load(scl + q * BT + t * kTileTokens, (q ? a.v_scale : a.k_scale) + r0, kTileTokens * 4, bars + t);
+        }
+    }
+    // other tiles: lane 4t + c issues box c's codes and scales of the part(s)
+    if (lane < 8 && row >= 0 && !(tb ? whole_1 : whole_0)) {
+        const int box = lane;
+        for (int q = p_lo; q <= p_hi; ++q) {
+            tma_load_2d(stage + q * CODES + box * kChunkTokens * D, q ? &a.v_map : &a.k_map, 0, row, bars + tb);
+            bulk_load(scl + q * BT + box * kChunkTokens, (q ? a.v_scale : a.k_scale) + row, kChunkTokens * 4,
+                      bars + tb);
         }
     }
 }
