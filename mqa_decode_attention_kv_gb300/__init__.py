@@ -30,7 +30,9 @@ MQA_DEV_TIMEOUT = 8
 MQA_MAX_SPLITS = 1024
 
 EXPORTED = ("kv_quant_append", "mqa_decode_attn", "mqa_decode_auto_splits", "mqa_decode_workspace_size",
-            "split_kv_combine", "mqa_prefill_attn", "mqa_status_str", "mqa_decode_attn_noalloc")
+            "split_kv_combine", "mqa_prefill_attn", "mqa_status_str", "mqa_decode_attn_noalloc",
+            "mqa_pc_create", "mqa_pc_destroy", "mqa_pc_match", "mqa_pc_insert", "mqa_pc_offload",
+            "mqa_pc_upload", "mqa_pc_stats")
 
 
 class MQAError(RuntimeError):
@@ -76,6 +78,21 @@ def declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.mqa_decode_attn_noalloc.restype = ctypes.c_int
     L.mqa_status_str.argtypes = [ctypes.c_int]
     L.mqa_status_str.restype = ctypes.c_char_p
+    i64 = ctypes.c_int64
+    L.mqa_pc_create.argtypes = [i32, i32, i32, i64, i32, P]
+    L.mqa_pc_create.restype = ctypes.c_int
+    L.mqa_pc_destroy.argtypes = [P]
+    L.mqa_pc_destroy.restype = None
+    L.mqa_pc_match.argtypes = [P, P, i64, P, i64]
+    L.mqa_pc_match.restype = i64
+    L.mqa_pc_insert.argtypes = [P, P, i64, P, P, i64]
+    L.mqa_pc_insert.restype = i64
+    L.mqa_pc_offload.argtypes = [P, P, i32, P, P, i64, P]
+    L.mqa_pc_offload.restype = ctypes.c_int
+    L.mqa_pc_upload.argtypes = [P, P, i32, P, P, i64, P]
+    L.mqa_pc_upload.restype = ctypes.c_int
+    L.mqa_pc_stats.argtypes = [P, P]
+    L.mqa_pc_stats.restype = ctypes.c_int
     return L
 
 
@@ -266,3 +283,73 @@ def mqa_prefill_attn(caches: Sequence[KVCache], layer_to_kv: Sequence[int], laye
                                 int(H), float(sm_scale), _ptr(dev_status), _stream(stream))
     _check("mqa_prefill_attn", rc)
     return out
+
+
+class PrefixCache:
+    """Host-memory prefix cache (mqa_prefix_cache.h): whole pages of every cache
+    of a layer stack, in a prefix tree keyed by a rolling hash of the tokens,
+    with LRU eviction of leaf pages.  ``pinned=False`` keeps only the tree
+    bookkeeping (no GPU needed; offload and upload are refused)."""
+
+    def __init__(self, page_size: int, head_dim: int, num_caches: int, host_pages: int, pinned: bool = True):
+        h = ctypes.c_void_p()
+        _check("mqa_pc_create", lib().mqa_pc_create(int(page_size), int(head_dim), int(num_caches),
+                                                    int(host_pages), int(bool(pinned)), ctypes.byref(h)))
+        self._h = h
+        self.page_size, self.head_dim, self.num_caches = int(page_size), int(head_dim), int(num_caches)
+
+    def close(self) -> None:
+        if self._h is not None and self._h.value:
+            lib().mqa_pc_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def match(self, tokens: np.ndarray) -> np.ndarray:
+        """Slots of the longest cached whole-page prefix of ``tokens`` (int32)."""
+        t = np.ascontiguousarray(tokens, np.int32)
+        cap = len(t) // self.page_size
+        slots = np.zeros(max(cap, 1), np.int64)
+        k = lib().mqa_pc_match(self._h, t.ctypes.data, len(t), slots.ctypes.data, cap)
+        if k < 0:
+            raise MQAError("mqa_pc_match", int(k))
+        return slots[:k].copy()
+
+    def insert(self, tokens: np.ndarray):
+        """Insert the whole pages of ``tokens``; returns (page indices, slots) of
+        the pages that are new (to be filled with ``offload``)."""
+        t = np.ascontiguousarray(tokens, np.int32)
+        cap = len(t) // self.page_size
+        idx = np.zeros(max(cap, 1), np.int64)
+        slots = np.zeros(max(cap, 1), np.int64)
+        n = lib().mqa_pc_insert(self._h, t.ctypes.data, len(t), idx.ctypes.data, slots.ctypes.data, cap)
+        if n < 0:
+            raise MQAError("mqa_pc_insert", int(n))
+        return idx[:n].copy(), slots[:n].copy()
+
+    def offload(self, caches, src_blocks, slots, stream=None) -> None:
+        """Device blocks -> pool slots (every cache), enqueued on ``stream``."""
+        b = np.ascontiguousarray(src_blocks, np.int32)
+        sl = np.ascontiguousarray(slots, np.int64)
+        assert len(b) == len(sl)
+        _check("mqa_pc_offload", lib().mqa_pc_offload(self._h, _caches_array(caches), len(caches), b.ctypes.data,
+                                                      sl.ctypes.data, len(b), _stream(stream)))
+
+    def upload(self, caches, slots, dst_blocks, stream=None) -> None:
+        """Pool slots -> device blocks (every cache), enqueued on ``stream``."""
+        b = np.ascontiguousarray(dst_blocks, np.int32)
+        sl = np.ascontiguousarray(slots, np.int64)
+        assert len(b) == len(sl)
+        _check("mqa_pc_upload", lib().mqa_pc_upload(self._h, _caches_array(caches), len(caches), sl.ctypes.data,
+                                                    b.ctypes.data, len(b), _stream(stream)))
+
+    def stats(self) -> dict:
+        out = np.zeros(8, np.int64)
+        _check("mqa_pc_stats", lib().mqa_pc_stats(self._h, out.ctypes.data))
+        keys = ("cached_pages", "free_slots", "capacity", "match_calls", "pages_matched", "pages_inserted",
+                "pages_evicted", "slot_bytes")
+        return dict(zip(keys, (int(x) for x in out)))

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmqa_kv.so")
 SOURCES = ["api.cu", "quant_append.cu", "decode.cu", "decode_tc.cu", "combine.cu", "prefill.cu", "prefill_tc.cu",
-           "no_alloc.cu"]
+           "no_alloc.cu", "prefix_cache.cu"]
 HEADERS = ["common.cuh", "kv_stage.cuh", "launch.h", "tc.cuh", "tc_pipe.cuh", "split_merge.cuh"]
 
 NVCC_FLAGS = [
@@ -41,6 +41,7 @@ def _nvcc() -> str:
 def _newest_input() -> float:
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     files.append(os.path.join(ROOT, "include", "mqa_kv.h"))
+    files.append(os.path.join(ROOT, "include", "mqa_prefix_cache.h"))
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

@@ -15,7 +15,8 @@ import mqa_decode_attention_kv_gb300 as mk
 from mqa_decode_attention_kv_gb300 import build as mkbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mqa_kv.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 FAKE = 0x10000  # a 16-byte aligned non-null "device" address, never dereferenced
 
 
@@ -26,7 +27,7 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)))
 
@@ -35,7 +36,7 @@ def test_exports_every_declared_symbol(L):
     names = declared_functions()
     assert set(names) >= {"kv_quant_append", "mqa_decode_attn", "mqa_prefill_attn", "split_kv_combine"}
     for n in names:
-        assert hasattr(L, n), f"{n} declared in mqa_kv.h but not exported"
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
     assert set(mk.EXPORTED) == set(names)
 
 
