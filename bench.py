@@ -389,6 +389,7 @@ class PrefillWorkload:
         prefix, new = w.len_values
         per = w.batch // w.groups
         pbs = synth.make_prefix_shared_batch(rng, w.groups, per, prefix, new, w.page_size)
+        self.pbs = pbs
         self.lens = pbs.seq_lens
         self.q_lens = np.full(w.batch, new, np.int64)
         D, H = w.head_dim, w.num_q_heads
@@ -658,6 +659,28 @@ def run_prefill(args, w):
     app_ms = statistics.mean(a.elapsed_time(b) for a, b in app)
     achieved = sum(wl.flops) / (sum(per_ms) * 1e-3) / 1e12
     append_bytes = wl.T * w.head_dim * 2 * 2 + wl.T * (2 * w.head_dim + 8)
+    # the step before prefill: a cached 8192-token prefix (128 pages) uploaded from the
+    # pinned host pool into device blocks (and offloaded once to fill the pool)
+    import mqa_decode_attention_kv_gb300 as mk
+    prefix = w.len_values[0]
+    n_pages = prefix // w.page_size
+    pc = mk.PrefixCache(w.page_size, w.head_dim, 1, host_pages=n_pages)
+    _, slots = pc.insert(np.arange(prefix, dtype=np.int32))
+    blocks = wl.pbs.block_table[0, :n_pages]
+    pc.offload([wl.cache], blocks, slots, stream=stream)
+    ups = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.roofline_reps + 1):
+            flush_l2(flush)
+            u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            pc.upload([wl.cache], slots, blocks, stream=stream)
+            u1.record(stream)
+            ups.append((u0, u1))
+    stream.synchronize()
+    up_ms = statistics.mean(a.elapsed_time(b) for a, b in ups[1:])
+    up_bytes = n_pages * pc.stats()["slot_bytes"]
+    pc.close()
     if rank != 0:
         return
     line = {
@@ -673,9 +696,91 @@ def run_prefill(args, w):
                      "kernel": "mqa_prefill_attn kernel, each call timed alone",
                      "ms_per_call": dict(zip([f"window_{x}" for x in w.windows], per_ms))},
         "append": {"ms": app_ms, "gbps": append_bytes / (app_ms * 1e6), "tokens": wl.T},
+        "prefix_upload": {"pages": n_pages, "bytes": up_bytes, "ms": up_ms, "gbps": up_bytes / (up_ms * 1e6),
+                          "how": "mqa_pc_upload of one cached 8192-token prefix from pinned host memory"},
         "gpu_launches": (1 + len(w.windows)) * args.steps,
         "clocks": clk.summary(),
     }
+    print(json.dumps(line), flush=True)
+
+
+def run_mixed(args):
+    """Continuous batching, one layer: 120 sequences decode one token while 8
+    prefill a 512-token chunk (lognormal contexts as in the 24-layer stack).
+    Times the whole batch as ONE mqa_prefill_attn launch (decode rows are
+    sequences with q_len = 1) against the same work as two launches (the decode
+    kernel over the 120 decode rows, the prefill kernel over the 8 chunks),
+    local window 1024 and global, L2 flushed before each."""
+    import torch
+    import mqa_decode_attention_kv_gb300 as mk
+    torch.cuda.set_device(0)
+    device = "cuda:0"
+    rng = np.random.default_rng(7)
+    n_dec, n_ch, chunk, H, D, P = 120, 8, 512, 32, 128, 64
+    ctx = np.clip(np.round(np.exp(rng.normal(np.log(4096.0), 1.0, n_dec + n_ch))), 1, 32768).astype(np.int64)
+    q_lens = np.concatenate([np.ones(n_dec, np.int64), np.full(n_ch, chunk, np.int64)])
+    lens = ctx.copy()
+    lens[n_dec:] += chunk
+    order = rng.permutation(n_dec + n_ch)
+    lens, q_lens = lens[order].astype(np.int32), q_lens[order]
+    pb = synth.make_paged_batch(rng, lens, P, shuffle=True)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(77)
+    cache = mk.KVCache.empty(pb.num_blocks, P, D, device=device)
+    cu_all = torch.from_numpy(synth.cu_from_counts(lens)).to(device)
+    T_all = int(lens.sum())
+    batch = mk.Batch.from_host(pb.block_table, lens, device=device)
+    mk.kv_quant_append(cache, batch, cu_all, T_all,
+                       torch.randn((T_all, D), generator=gen, device=device).to(torch.bfloat16),
+                       torch.randn((T_all, D), generator=gen, device=device).to(torch.bfloat16))
+    cu_q = torch.from_numpy(synth.cu_from_counts(q_lens)).to(device)
+    T = int(q_lens.sum())
+    q = torch.randn((T, H, D), generator=gen, device=device).to(torch.bfloat16)
+    dec = np.nonzero(q_lens == 1)[0]
+    chs = np.nonzero(q_lens > 1)[0]
+    b_dec = mk.Batch.from_host(np.ascontiguousarray(pb.block_table[dec]), lens[dec], device=device)
+    b_ch = mk.Batch.from_host(np.ascontiguousarray(pb.block_table[chs]), lens[chs], device=device)
+    cu_ch = torch.from_numpy(synth.cu_from_counts(q_lens[chs])).to(device)
+    q_dec = q[torch.from_numpy(synth.cu_from_counts(q_lens)[dec]).to(device)].contiguous()
+    rows_ch = np.concatenate([np.arange(synth.cu_from_counts(q_lens)[b], synth.cu_from_counts(q_lens)[b + 1])
+                              for b in chs])
+    q_ch = q[torch.from_numpy(rows_ch).to(device)].contiguous()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device=device)
+    res = {}
+    with torch.cuda.stream(stream):
+        for W in (1024, 0):
+            ws = None
+            splits = mk.mqa_decode_auto_splits(b_dec, W, H, D, P)
+            if splits > 1:
+                ws = torch.empty(mk.mqa_decode_workspace_size(len(dec), H, D, splits), dtype=torch.uint8,
+                                 device=device)
+            one = lambda: mk.mqa_prefill_attn([cache], [0], 0, W, batch, cu_q, q, chunk, stream=stream)
+            two = lambda: (mk.mqa_decode_attn([cache], [0], 0, W, b_dec, q_dec, num_splits=splits, workspace=ws,
+                                              stream=stream),
+                           mk.mqa_prefill_attn([cache], [0], 0, W, b_ch, cu_ch, q_ch, chunk, stream=stream))
+            for name, fn in (("one_launch", one), ("two_launches", two)):
+                for _ in range(max(args.warmup, 1)):
+                    fn()
+                ts = []
+                for _ in range(args.steps):
+                    flush_l2(flush)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    ts.append((e0, e1))
+                stream.synchronize()
+                res[f"window_{W}_{name}_ms"] = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    line = {"metric": "mixed decode + prefill-chunk batch attention ms per layer on 1 GB300",
+            "value": res["window_1024_one_launch_ms"], "unit": "ms", "higher_is_better": False,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "i8kv-f16mma-f32acc",
+            "data": "synthetic",
+            "config": {"workload": f"mixed_b128: {n_dec} decode rows + {n_ch} prefill chunks of {chunk} tokens, "
+                                   f"32 q heads, d=128, page 64, ctx lognormal (4096, 1.0, 32768) "
+                                   f"(mean {float(lens.mean()):.0f})", "tokens": T,
+                       "l2": "L2 flushed (512 MB read) before every timed call"},
+            "times": res}
     print(json.dumps(line), flush=True)
 
 
@@ -699,7 +804,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="stack24_b128", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", default="stack24_b128", choices=sorted(synth.CONFIGS) + ["mixed_b128"])
     ap.add_argument("--roofline-reps", type=int, default=3)
     ap.add_argument("--cpu-seqs", type=int, default=32, help="sequences in the cpu_baseline's timed sample")
     ap.add_argument("--ref-seqs", type=int, default=4,
@@ -711,6 +816,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be >= 3")
+    if args.workload == "mixed_b128":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle baseline covers decode workloads only"}))
+            return
+        from mqa_decode_attention_kv_gb300 import build as _b
+        _b.build()
+        run_mixed(args)
+        return
     w = synth.CONFIGS[args.workload]
     if args.impl == "reference":
         if w.name == "prefix_prefill":

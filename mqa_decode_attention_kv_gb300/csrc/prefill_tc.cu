@@ -184,8 +184,6 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.num_q_heads;
     const int tpc = C::M / H;  // query tokens per CTA
-    const int b = blockIdx.y;
-    const int t_begin = blockIdx.x * tpc;
 
     // ---- set-up (no global memory: overlaps the previous kernel)
     if (tid == 0) {
@@ -209,14 +207,70 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
     griddep_wait();
     griddep_launch_dependents();
 
+    // ---- this CTA's tile: CTA x takes tile x of the list of every sequence's
+    // ceil(q_len / tpc) tiles (a mixed batch of decode rows, q_len = 1, and long
+    // prefill chunks launches no idle CTA per sequence); a block-wide scan of cu_q
+    __shared__ int pf_scan[C::THREADS / 32 + 2];
+    {
+        if (tid == 0)
+            pf_scan[C::THREADS / 32] = -1;
+        long long run = 0;
+        const long long x = blockIdx.x;
+        for (int b0 = 0; b0 < a.batch; b0 += C::THREADS) {
+            const int bb = b0 + tid;
+            int nt = 0;
+            if (bb < a.batch) {
+                const int ql = __ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb);
+                nt = ql > 0 ? (ql + tpc - 1) / tpc : 0;
+            }
+            int incl = nt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off)
+                    incl += y;
+            }
+            __syncthreads();  // pf_scan reuse
+            if (lane == 31)
+                pf_scan[warp] = incl;
+            __syncthreads();
+            long long pre = run, chunk = 0;
+            for (int w = 0; w < C::THREADS / 32; ++w) {
+                if (w < warp)
+                    pre += pf_scan[w];
+                chunk += pf_scan[w];
+            }
+            const long long lo_t = pre + incl - nt;
+            if (nt > 0 && lo_t <= x && x < lo_t + nt) {
+                pf_scan[C::THREADS / 32] = bb;
+                pf_scan[C::THREADS / 32 + 1] = (int)(x - lo_t);
+            }
+            run += chunk;
+        }
+        __syncthreads();
+    }
+    const bool past_end = pf_scan[C::THREADS / 32] < 0;  // beyond the last tile: leaves below
+    const int b = past_end ? 0 : pf_scan[C::THREADS / 32];
+    const int t_begin = past_end ? 0 : pf_scan[C::THREADS / 32 + 1] * tpc;
+    if (blockIdx.x == 0) {
+        // one CTA reports bad lengths and query counts of the whole batch (a sequence with
+        // q_len <= 0 gets no tile)
+        for (int bb = tid; bb < a.batch; bb += C::THREADS) {
+            const int Lb = __ldg(a.seq_lens + bb);
+            const int qa = __ldg(a.cu_q + bb), qb = __ldg(a.cu_q + bb + 1);
+            if (Lb < 1 || Lb > a.max_seq_len)
+                set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);
+            else if (qb - qa > Lb || qa < 0 || qb < qa || qb > a.total_q)
+                set_status(a.dev_status, MQA_DEV_BAD_CU);
+        }
+    }
+
     // ---- this CTA's rows and keys (every thread computes the same)
     const int L = __ldg(a.seq_lens + b);
     const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
     const int qlen = q1 - q0;
     const bool bad = L < 1 || L > a.max_seq_len || qlen > L || q0 < 0 || qlen < 0 || q1 > a.total_q;
-    if (bad && tid == 0 && blockIdx.x == 0)
-        set_status(a.dev_status, (L < 1 || L > a.max_seq_len) ? MQA_DEV_BAD_SEQLEN : MQA_DEV_BAD_CU);
-    const int ntok = bad ? 0 : min(qlen, t_begin + tpc) - t_begin;  // query tokens of this CTA
+    const int ntok = (bad || past_end) ? 0 : min(qlen, t_begin + tpc) - t_begin;  // query tokens of this CTA
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -690,8 +744,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s)
             return cudaErrorInvalidConfiguration;
         attr_set.store(1, std::memory_order_release);
     }
+    // an upper bound of the tiles (sum over sequences of ceil(q_len / tpc)); CTAs past the
+    // last tile leave at once
     const int tpc = PfCfg::M / a.num_q_heads;
-    dim3 grid((unsigned)((a.max_q_len + tpc - 1) / tpc), (unsigned)a.batch, 1);
+    const long long tiles = ((long long)a.total_q + tpc - 1) / tpc + a.batch;
+    if (tiles > 0x7fffffffll)
+        return cudaErrorInvalidConfiguration;
+    dim3 grid((unsigned)tiles, 1, 1);
     return launch_pdl(prefill_tc_kernel, grid, dim3(PfCfg::THREADS), PfCfg::SMEM_BYTES, s, a);
 }
 

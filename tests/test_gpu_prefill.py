@@ -6,7 +6,7 @@ import torch
 import oracle
 import synth
 import mqa_decode_attention_kv_gb300 as mk
-from gpu_common import assert_close, caches_equal, sm_scale, to_dev_bf16, to_dev_i32
+from gpu_common import assert_close, build_caches, caches_equal, sm_scale, to_dev_bf16, to_dev_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -85,3 +85,41 @@ def test_prefill_prefix_reuse_full_size_sampled():
     for window in w.windows:
         got, ref = run(st, window, rows)
         assert_close(got, ref, f"prefix_prefill W={window}")
+
+
+@pytest.mark.parametrize("num_decode,chunks", [(36, [64, 200, 1, 513]), (600, [3, 130])])
+def test_mixed_decode_rows_and_prefill_chunks_one_launch(num_decode, chunks):
+    """Continuous batching (LLM-inference workshop transcript, 01:03:27-01:04:33):
+    one mqa_prefill_attn launch over sequences that decode one token (q_len = 1)
+    next to sequences that prefill a chunk; every row against the oracle, the
+    decode rows also against the decode kernel.  600 sequences take the tile
+    scan over more than one pass of the CTA."""
+    rng = np.random.default_rng(num_decode)
+    H, d, page = 32, 128, 64
+    dec_lens = rng.integers(1, 700 if num_decode < 100 else 200, num_decode)
+    ch_q = np.asarray(chunks, np.int64)
+    ch_lens = ch_q + rng.integers(0, 300, len(chunks))
+    lens = np.concatenate([dec_lens, ch_lens]).astype(np.int32)
+    q_lens = np.concatenate([np.ones(num_decode, np.int64), ch_q])
+    order = rng.permutation(len(lens))  # decode rows and chunks interleaved in the batch
+    lens, q_lens = lens[order], q_lens[order]
+    st = build_caches(rng, lens, page, d, 1)
+    cu_q = synth.cu_from_counts(q_lens)
+    T = int(cu_q[-1])
+    q_bits = synth.bf16_normal(rng, (T, H, d))
+    q_dev = to_dev_bf16(q_bits)
+    for window in (0, 100, 1024):
+        out = mk.mqa_prefill_attn(st.gpu_caches, [0], 0, window, st.batch, to_dev_i32(cu_q), q_dev,
+                                  int(q_lens.max()), sm_scale=sm_scale(d))
+        torch.cuda.synchronize()
+        rs, rp = oracle.prefill_rows(cu_q, lens)
+        ref, _ = oracle.attention(st.ora_caches[0], st.pb.block_table, lens, q_bits, rs, rp, window, sm_scale(d))
+        assert_close(out, ref, f"mixed batch W={window}")
+        # the decode rows through the decode kernel agree with the same rows of the mixed launch
+        dec = np.nonzero(q_lens == 1)[0]
+        rows = torch.from_numpy(cu_q[dec].astype(np.int64)).cuda()
+        qd = torch.zeros((len(lens), H, d), dtype=torch.bfloat16, device="cuda")
+        qd[torch.from_numpy(dec).cuda()] = q_dev[rows]
+        od = mk.mqa_decode_attn(st.gpu_caches, [0], 0, window, st.batch, qd, sm_scale=sm_scale(d))
+        torch.cuda.synchronize()
+        assert_close(od[torch.from_numpy(dec).cuda()], ref[cu_q[dec]], f"decode kernel rows W={window}")
