@@ -626,8 +626,9 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 const float ksv = fetched ? scl[r * 2 * BT + tok] : 0.f;
                 const float vsv = fetched ? scl[r * 2 * BT + BT + tok] : 0.f;
                 // ---- K: 128 codes -> fp16 pairs in tensor memory (lane tok, 64 columns); the
-                // group's K buffer was last read by S^T of its previous block, which it waited for
-#pragma unroll
+                // group's K buffer was last read by S^T of its previous block, which it waited for.
+                // (A loop, not unrolled: the kernel's instruction footprint is a bottleneck of its own.)
+#pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     uint4 kc[4];
 #pragma unroll

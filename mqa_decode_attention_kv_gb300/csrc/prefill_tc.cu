@@ -558,7 +558,8 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             const uint8_t *crow = st + kr * D;
             // ---- K: 128 codes -> fp16 (+1152) into K buffer b2, row kr
             uint8_t *kh = kh0 + b2 * BK * D * 2;
-#pragma unroll
+            // (a loop, not unrolled: the kernel's instruction footprint is a bottleneck of its own)
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 uint4 kc[4];
 #pragma unroll
