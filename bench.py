@@ -784,6 +784,97 @@ def run_mixed(args):
     print(json.dumps(line), flush=True)
 
 
+_MMA_RATE_SRC = r"""
+// Warp-level MMA throughput: int8 m16n8k32 (s32 accumulate) against fp16 m16n8k16 (fp32
+// accumulate), eight independent accumulators per warp, registers only.
+#include <cstdio>
+#include <cstdint>
+#include <cuda_runtime.h>
+template <bool I8>
+__global__ void __launch_bounds__(256) rate(long long *out, int iters) {
+    uint32_t a[4] = {threadIdx.x, threadIdx.x * 3u, 7u, 9u}, b[2] = {5u, threadIdx.x};
+    float f[8][4] = {};
+    int s[8][4] = {};
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (I8)
+                asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                             : "+r"(s[k][0]), "+r"(s[k][1]), "+r"(s[k][2]), "+r"(s[k][3])
+                             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+            else
+                asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                             : "+f"(f[k][0]), "+f"(f[k][1]), "+f"(f[k][2]), "+f"(f[k][3])
+                             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+        }
+    }
+    float acc = 0.f;
+    for (int k = 0; k < 8; ++k) for (int q = 0; q < 4; ++q) acc += f[k][q] + (float)s[k][q];
+    if (acc == 12345.f) out[0] = 1;
+}
+int main() {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+    long long *d;
+    cudaMalloc(&d, 8);
+    const int iters = 4096, blocks = sms * 4;
+    for (int i8 = 0; i8 < 2; ++i8) {
+        cudaEvent_t e0, e1;
+        cudaEventCreate(&e0);
+        cudaEventCreate(&e1);
+        float ms = 0.f;
+        for (int rep = 0; rep < 3; ++rep) {
+            cudaEventRecord(e0);
+            if (i8) rate<true><<<blocks, 256>>>(d, iters); else rate<false><<<blocks, 256>>>(d, iters);
+            cudaEventRecord(e1);
+            cudaEventSynchronize(e1);
+            cudaEventElapsedTime(&ms, e0, e1);
+        }
+        const double ops = (double)blocks * 8 * iters * 8 * (i8 ? 8192.0 : 4096.0);
+        printf("%s %.1f %s\n", i8 ? "int8_m16n8k32_tops" : "fp16_m16n8k16_tflops", ops / (ms * 1e9),
+               cudaGetErrorString(cudaGetLastError()));
+    }
+    return 0;
+}
+"""
+
+_KIND_I8_SRC = r"""
+#include <cstdint>
+__global__ void k(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred pa;\n\tsetp.ne.b32 pa, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::i8 [%0], %1, %2, %3, pa;\n\t}" ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(1u));
+}
+"""
+
+
+def run_mma_rates(args):
+    """The int8-MMA question (fully int8 attention only pays if int8 MMA beats
+    fp16 here): whether ptxas accepts tcgen05.mma kind::i8 for sm_103a, and the
+    measured warp-level int8 and fp16 MMA rates of this GPU."""
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    out = {"metric": "warp-level MMA rates (int8 vs fp16) and tcgen05 kind::i8 availability on 1 GB300"}
+    with tempfile.TemporaryDirectory() as tmp:
+        src = os.path.join(tmp, "i8.cu")
+        open(src, "w").write(_KIND_I8_SRC)
+        r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-c", src, "-o",
+                            os.path.join(tmp, "i8.o")], capture_output=True, text=True)
+        msg = [l for l in (r.stdout + r.stderr).splitlines() if "error" in l]
+        out["tcgen05_kind_i8_sm_103a"] = {"compiles": r.returncode == 0,
+                                          "ptxas": msg[0].split("error")[-1].strip(" :") if msg else ""}
+        src = os.path.join(tmp, "rate.cu")
+        open(src, "w").write(_MMA_RATE_SRC)
+        exe = os.path.join(tmp, "rate")
+        subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", src, "-o", exe])
+        res = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+        for line in res:
+            parts = line.split()
+            if len(parts) >= 3:
+                out[parts[0]] = float(parts[1])
+                assert parts[2] == "no", line
+    print(json.dumps(out), flush=True)
+
+
 def run_profile(args, w):
     """Set-up plus a few eager steps, nothing else: a short, bounded program
     for ncu (one GPU)."""
@@ -804,7 +895,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="stack24_b128", choices=sorted(synth.CONFIGS) + ["mixed_b128"])
+    ap.add_argument("--workload", default="stack24_b128", choices=sorted(synth.CONFIGS) + ["mixed_b128", "mma_rates"])
     ap.add_argument("--roofline-reps", type=int, default=3)
     ap.add_argument("--cpu-seqs", type=int, default=32, help="sequences in the cpu_baseline's timed sample")
     ap.add_argument("--ref-seqs", type=int, default=4,
@@ -816,6 +907,12 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be >= 3")
+    if args.workload == "mma_rates":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "a hardware-rate probe has no reference arm"}))
+            return
+        run_mma_rates(args)
+        return
     if args.workload == "mixed_b128":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the oracle baseline covers decode workloads only"}))
