@@ -162,6 +162,14 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Hint: bring the line holding p into L2 (no data returns to the thread).  L2 is
+// the point of coherence, so this may run before griddep_wait(): a line the
+// predecessor writes afterwards is updated there, never served stale.
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- TMA
 // 2-D tiled load of one box into shared memory; completion is signalled on
 // `bar` as transaction bytes.

@@ -316,6 +316,21 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.v_map64 : &a.v_map))
                      : "memory");
     }
+    if (warp == C::THREADS / 32 - 1) {
+        // while the previous kernel may still run: warm L2 with the lengths and, in whole-pair
+        // mode, this CTA's block-table row and query rows (the first three things it reads)
+        for (int off = lane * 128; off < a.batch * 4; off += 32 * 128)
+            prefetch_l2(reinterpret_cast<const char *>(a.seq_lens) + off);
+        if (!balanced) {
+            const int bb = cta / groups, gg = cta % groups;
+            const char *row = reinterpret_cast<const char *>(a.block_table + (size_t)bb * a.max_blocks);
+            for (int off = lane * 128; off < a.max_blocks * 4 && off < 64 * 128; off += 32 * 128)
+                prefetch_l2(row + off);
+            const char *qp = reinterpret_cast<const char *>(a.q + ((size_t)bb * a.num_q_heads + gg * NH) * D);
+            for (int off = lane * 128; off < NH * D * 2; off += 32 * 128)
+                prefetch_l2(qp + off);
+        }
+    }
     // the previous kernel's writes (the cache slot just appended, q, out, the workspace) are visible from here
     griddep_wait();
     griddep_launch_dependents();

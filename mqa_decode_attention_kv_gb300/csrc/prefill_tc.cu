@@ -108,42 +108,6 @@ static_assert(128 * (3 * PfCfg::REG_WORK + PfCfg::REG_CTRL) <= PfCfg::REG_LAUNCH
 
 constexpr float kBiasK = 1152.f;  // K codes enter the tensor core as code + 1152 (exact in fp16)
 
-// Packed fp32 pairs (one instruction for two lanes of arithmetic) and a 3-input maximum.
-__device__ __forceinline__ uint64_t f2pack(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ float max3f(float a, float b, float c)
-{
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
 // The key range of a CTA as the TMA helpers see it: blocks of two 64-token
 // tiles from tile t_first, keys [lo, L).
 struct PfPos {
