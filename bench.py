@@ -138,9 +138,12 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU workloads
 class DecodeStack:
-    """Caches, inputs and pre-marshalled C-ABI arguments of a decode step."""
+    """Caches, inputs and pre-marshalled C-ABI arguments of a decode step.
+    ring_local: caches read only by local layers are window-bounded rings of
+    (W-1)/P + 2 pages per sequence (page p in table entry p % R); the global
+    caches keep full tables."""
 
-    def __init__(self, w: "synth.Workload", device):
+    def __init__(self, w: "synth.Workload", device, ring_local: bool = False):
         import ctypes
         import torch
         import mqa_decode_attention_kv_gb300 as mk
@@ -154,21 +157,48 @@ class DecodeStack:
         gen.manual_seed(1000 + w.seed)
         T = int(self.lens.sum())
         cu_all = torch.from_numpy(synth.cu_from_counts(self.lens)).to(device)
+        # which caches are read by local layers only (candidates for rings)
+        local_only = [all(w.windows[l] > 0 for l in range(w.num_layers) if w.layer_map[l] == c)
+                      for c in range(w.num_caches)]
+        self.ring = 0
+        self.ring_batch = None
+        self.cache_is_ring = [False] * w.num_caches
+        if ring_local and any(local_only):
+            wmax = max(w.windows[l] for l in range(w.num_layers) if local_only[w.layer_map[l]])
+            self.ring = (wmax - 1) // P + 2
+            table = rng.permutation(B * self.ring).astype(np.int32).reshape(B, self.ring)
+            self.ring_batch = mk.Batch.from_host(table, self.lens, device=device, ring_blocks=self.ring)
+            self.cache_is_ring = list(local_only)
+            # the resident tokens of each sequence: its last pages, at most ring pages
+            first_res = np.maximum(0, ((self.lens.astype(np.int64) - 1) // P - (self.ring - 1)) * P)
+            res_counts = (self.lens - first_res).astype(np.int64)
+            cu_res = torch.from_numpy(synth.cu_from_counts(res_counts)).to(device)
+            T_res = int(res_counts.sum())
+            cu_host = synth.cu_from_counts(self.lens)
+            res_rows = torch.from_numpy(np.concatenate([np.arange(int(cu_host[b + 1]) - int(res_counts[b]),
+                                                                  int(cu_host[b + 1])) for b in range(B)])).to(device)
         self.caches = []
-        for _ in range(w.num_caches):
-            c = mk.KVCache.empty(self.pb.num_blocks, P, D, device=device)
+        for c_i in range(w.num_caches):
             k = torch.randn((T, D), generator=gen, device=device).to(torch.bfloat16)
             v = torch.randn((T, D), generator=gen, device=device).to(torch.bfloat16)
-            mk.kv_quant_append(c, self.batch, cu_all, T, k, v)
+            if self.cache_is_ring[c_i]:
+                c = mk.KVCache.empty(B * self.ring, P, D, device=device)
+                mk.kv_quant_append(c, self.ring_batch, cu_res, T_res, k[res_rows].contiguous(),
+                                   v[res_rows].contiguous())
+            else:
+                c = mk.KVCache.empty(self.pb.num_blocks, P, D, device=device)
+                mk.kv_quant_append(c, self.batch, cu_all, T, k, v)
             del k, v
             self.caches.append(c)
+        self.pool_bytes = sum(c.k_codes.numel() * 2 + c.k_scale.numel() * 8 for c in self.caches)
+        self.full_pool_bytes = w.num_caches * self.pb.num_blocks * P * 2 * (D + 4)
         L = w.num_layers
         self.q = torch.randn((L, B, H, D), generator=gen, device=device).to(torch.bfloat16)
         self.k_new = torch.randn((w.num_caches, B, D), generator=gen, device=device).to(torch.bfloat16)
         self.v_new = torch.randn((w.num_caches, B, D), generator=gen, device=device).to(torch.bfloat16)
         self.out = torch.empty_like(self.q)
         self.cu_step = torch.arange(B + 1, dtype=torch.int32, device=device)
-        self.splits = [mk.mqa_decode_auto_splits(self.batch, w.windows[l], H, D, P) for l in range(L)]
+        self.splits = [mk.mqa_decode_auto_splits(self.batch_of_layer(l), w.windows[l], H, D, P) for l in range(L)]
         ws = max(mk.mqa_decode_workspace_size(B, H, D, s) for s in self.splits)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         # device-side error bits of every call (bad inputs, a bounded wait that ran out)
@@ -181,30 +211,38 @@ class DecodeStack:
         self._carr = mk._caches_array(self.caches)
         self._lmap = (ctypes.c_int32 * L)(*w.layer_map)
         self._bt = self.batch.c()
+        self._bt_ring = self.ring_batch.c() if self.ring_batch is not None else None
         self._cptr = [ctypes.byref(self._carr[i]) for i in range(len(self.caches))]
         self.scale = 1.0 / math.sqrt(D)
         self.lib = mk.lib()
         self.bytes_per_layer = [acc.decode_kv_bytes(self.lens, w.windows[l], D) for l in range(L)]
         self.flops_per_layer = [acc.decode_flops(self.lens, w.windows[l], H, D) for l in range(L)]
 
+    def batch_of_cache(self, c: int):
+        return self.ring_batch if self.cache_is_ring[c] else self.batch
+
+    def batch_of_layer(self, l: int):
+        return self.batch_of_cache(self.w.layer_map[l])
+
+    def _bt_of_cache(self, c: int):
+        return self._bt_ring if self.cache_is_ring[c] else self._bt
+
     def launches_per_step(self) -> int:
         return len(self.append_before) + sum(2 if s > 1 else 1 for s in self.splits)
 
     def append(self, c: int, stream: int):
         B = self.w.batch
-        rc = self.lib.kv_quant_append(self._cptr[c], self.torch_ptr_bt(), self.cu_step.data_ptr(), B,
+        import ctypes
+        rc = self.lib.kv_quant_append(self._cptr[c], ctypes.byref(self._bt_of_cache(c)), self.cu_step.data_ptr(), B,
                                       self.k_new[c].data_ptr(), self.v_new[c].data_ptr(), None, stream)
         assert rc == 0, rc
-
-    def torch_ptr_bt(self):
-        import ctypes
-        return ctypes.byref(self._bt)
 
     def attend(self, l: int, stream: int):
         import ctypes
         w = self.w
         rc = self.lib.mqa_decode_attn(self._carr, len(self.caches), self._lmap, w.num_layers, l, w.windows[l],
-                                      ctypes.byref(self._bt), self.q[l].data_ptr(), self.out[l].data_ptr(),
+                                      ctypes.byref(self._bt_of_cache(w.layer_map[l])), self.q[l].data_ptr(),
+                                      self.out[l].data_ptr(),
                                       w.num_q_heads, self.scale, self.splits[l], self.ws.data_ptr(),
                                       self.ws.numel(), ctypes.c_void_p(self.status.data_ptr()), stream)
         assert rc == 0, rc
@@ -305,9 +343,9 @@ def e2e_steps(stack: DecodeStack, steps, stream, graph: bool):
         for l in range(w.num_layers):
             c = stack.append_before.get(l)
             if c is not None:
-                mk.kv_quant_append(stack.caches[c], stack.batch, stack.cu_step, w.batch, kn_dev[c], vn_dev[c],
-                                   stream=s)
-            mk.mqa_decode_attn(stack.caches, list(w.layer_map), l, w.windows[l], stack.batch, q_dev[l],
+                mk.kv_quant_append(stack.caches[c], stack.batch_of_cache(c), stack.cu_step, w.batch, kn_dev[c],
+                                   vn_dev[c], stream=s)
+            mk.mqa_decode_attn(stack.caches, list(w.layer_map), l, w.windows[l], stack.batch_of_layer(l), q_dev[l],
                                out=out_dev[l], num_splits=stack.splits[l], workspace=stack.ws, stream=s)
         out_host.copy_(out_dev, non_blocking=True)
 
@@ -331,9 +369,9 @@ def e2e_steps(stack: DecodeStack, steps, stream, graph: bool):
             s.wait_event(q_in[l])
             c = stack.append_before.get(l)
             if c is not None:
-                mk.kv_quant_append(stack.caches[c], stack.batch, stack.cu_step, w.batch, kn_dev[c], vn_dev[c],
-                                   stream=s)
-            mk.mqa_decode_attn(stack.caches, list(w.layer_map), l, w.windows[l], stack.batch, q_dev[l],
+                mk.kv_quant_append(stack.caches[c], stack.batch_of_cache(c), stack.cu_step, w.batch, kn_dev[c],
+                                   vn_dev[c], stream=s)
+            mk.mqa_decode_attn(stack.caches, list(w.layer_map), l, w.windows[l], stack.batch_of_layer(l), q_dev[l],
                                out=out_dev[l], num_splits=stack.splits[l], workspace=stack.ws, stream=s)
             done = torch.cuda.Event()
             done.record(s)
@@ -559,7 +597,7 @@ def run_decode(args, w):
     device = f"cuda:{local_rank}"
     torch.cuda.set_device(local_rank)
     hbm, bf16, bf16_sus, peak_kind = measured_peaks()
-    stack = DecodeStack(w, device)
+    stack = DecodeStack(w, device, ring_local=args.ring_local)
     stream = torch.cuda.Stream(device=device)
     sptr = stream.cuda_stream
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
@@ -611,7 +649,8 @@ def run_decode(args, w):
                             "mqa_decode_attention_kv_gb300/csrc/decode.cu",
                             "mqa_decode_attention_kv_gb300/csrc/kv_stage.cuh",
                             "mqa_decode_attention_kv_gb300/csrc/common.cuh"])
-    traffic = profile_traffic(f"decode_{w.name}_traffic.txt", digest)
+    # the committed capture is of the full-table step
+    traffic = None if args.ring_local else profile_traffic(f"decode_{w.name}_traffic.txt", digest)
     e2e = None
     if not args.no_e2e:
         n_e2e = max(3, min(args.steps, 10))
@@ -642,7 +681,10 @@ def run_decode(args, w):
                           "(nothing runs between them), so kv_gbps is not an HBM figure; step_layers_cold and "
                           "roofline time every layer with L2 flushed before it"),
                    "timing": "CUDA graph of the whole step, replayed; CUDA events on the launching stream",
-                   "kv_bytes_per_step": kv_bytes, "kv_gbps": kv_bytes / (ms * 1e6)},
+                   "kv_bytes_per_step": kv_bytes, "kv_gbps": kv_bytes / (ms * 1e6),
+                   "local_caches": (f"window-bounded rings of {stack.ring} pages per sequence" if stack.ring
+                                    else "full block tables"),
+                   "kv_pool_bytes": stack.pool_bytes, "kv_pool_bytes_full_tables": stack.full_pool_bytes},
         "step_layers_cold": {"ms_per_step": seg_ms, "tokens_per_s": world * B / (seg_ms / 1000.0),
                              "kv_gbps": kv_bytes / (seg_ms * 1e6),
                              "how": "sum over the 24 layers of (append if any + decode call), each timed alone "
@@ -960,6 +1002,8 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=4,
                     help="sequences per step of the reference arm (the oracle on the host cores)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ring-local", action="store_true",
+                    help="decode workloads: caches read only by local layers as window-bounded rings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="set up the workload, run --steps eager steps and exit (for ncu captures)")
