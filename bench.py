@@ -646,7 +646,7 @@ def run_decode(args, w):
                 "splits": sorted(set(stack.splits[l] for l in ls))}
 
     digest = source_digest(["mqa_decode_attention_kv_gb300/csrc/decode_tc.cu",
-                            "mqa_decode_attention_kv_gb300/csrc/decode.cu",
+                            "mqa_decode_attention_kv_gb300/csrc/tc_pipe.cuh",
                             "mqa_decode_attention_kv_gb300/csrc/kv_stage.cuh",
                             "mqa_decode_attention_kv_gb300/csrc/common.cuh"])
     # the committed capture is of the full-table step

@@ -139,8 +139,10 @@ int kv_quant_append(const mqa_kv_cache *cache, const mqa_batch *batch, const int
  *   q:   bf16 [batch][num_q_heads][head_dim], 16-byte aligned.  sm_scale > 0.
  *   out: bf16 [batch][num_q_heads][head_dim], 16-byte aligned.
  *   num_splits: 0 = choose automatically (see mqa_decode_auto_splits), 1 = one
- *        CTA per sequence, S > 1 = up to S key ranges per sequence processed in
- *        parallel and merged by split_kv_combine (flash-decoding).
+ *        CTA per (sequence, head group), S > 1 = the (sequence, head group, key
+ *        block) list cut into equal shares over up to batch * groups * S / 2
+ *        CTAs; a pair cut between CTAs is merged from its pieces' partials
+ *        (flash-decoding).
  *   workspace: device scratch of at least
  *        mqa_decode_workspace_size(batch, num_q_heads, head_dim, S) bytes
  *        (16-byte aligned) when the effective split count S exceeds 1; may be
@@ -156,15 +158,14 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
 int mqa_decode_auto_splits(const mqa_batch *batch, int32_t window, int32_t num_q_heads, int32_t head_dim,
                            int32_t page_size);
 
-/* Bytes of decode workspace for `num_splits` splits: fp32 partial outputs
- * [batch][num_splits][num_q_heads][head_dim], then fp32 log-sum-exps
- * [batch][num_splits][num_q_heads], then max(one int32 ticket per (sequence,
- * group of 32 heads), 64 KiB of merge descriptors), each region 256-byte
- * aligned.  0 when num_splits <= 1.  head_dim 128 with 32 or 64 heads runs the
- * tcgen05 kernel, which writes its partials and merge descriptors there and
- * merges them in a second kernel; otherwise with at most 16 splits the decode
- * kernel merges the partials itself (the tickets are zeroed on the stream
- * first), and wider splits run split_kv_combine. */
+/* Bytes of decode workspace for `num_splits` splits: room for fp32 partial
+ * outputs [batch][num_splits][num_q_heads][head_dim], then fp32 log-sum-exps
+ * [batch][num_splits][num_q_heads], then 64 KiB of merge descriptors, each
+ * region 256-byte aligned.  0 when num_splits <= 1.  With S splits the decode
+ * runs balanced shares over at most batch * groups * S / 2 CTAs (a group is 32
+ * query heads at head_dim 128, 16 at head_dim 64), each keeping the partials of
+ * the two (sequence, head group) pairs it may share with its neighbours there;
+ * a second kernel merges them. */
 size_t mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t head_dim, int32_t num_splits);
 
 /* Merge split-KV partial results (flash-decoding combine; the same log-sum-exp

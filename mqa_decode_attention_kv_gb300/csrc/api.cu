@@ -13,8 +13,6 @@ using namespace mqa;
 
 namespace {
 
-constexpr int kMinTilesPerSplit = 2;  // below this a split's fixed costs dominate
-
 bool aligned16(const void *p)
 {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -135,14 +133,13 @@ int sm_count()
     return n;
 }
 
-int ctas_per_sm(int head_dim, int heads)
+int tc_ctas_per_sm()
 {
-    static std::atomic<int> cached[4];
-    const int idx = (head_dim == 128 ? 2 : 0) + (heads <= 16 ? 0 : 1);
-    int v = cached[idx].load(std::memory_order_relaxed);
+    static std::atomic<int> cached{0};
+    int v = cached.load(std::memory_order_relaxed);
     if (v <= 0) {
-        v = decode_ctas_per_sm(head_dim, heads);
-        cached[idx].store(v, std::memory_order_relaxed);
+        v = decode_tc_ctas_per_sm();
+        cached.store(v, std::memory_order_relaxed);
     }
     return v;
 }
@@ -152,66 +149,6 @@ int tiles_for(int L, int W)
 {
     const int lo = (W > 0 && L > W) ? L - W : 0;
     return (L - 1) / kTileTokens - lo / kTileTokens + 1;
-}
-
-// The balanced (persistent) tensor-core decode: CTAs it runs at most, and the
-// split count whose workspace holds its partials (2 slots of 32 heads per CTA).
-int tc_max_ctas(int head_dim, int heads)
-{
-    const int sms = sm_count();
-    if (sms <= 0)
-        return 0;
-    const int g = sms * ctas_per_sm(head_dim, heads);
-    return g < kTcMaxCtas ? g : kTcMaxCtas;
-}
-
-// 64-token tiles of a decode key range; defined below.
-int tiles_for(int L, int W);
-int tiles_bound(int Lmax, int W);
-
-// Whether the automatic plan of the tcgen05 kernel runs one CTA per (sequence,
-// head group) instead of balanced shares.  Cutting a pair between CTAs costs
-// far more than its blocks (the pieces' epilogues and reference moves, the
-// merge kernel): measured on GB300, a 24-layer step ran 17% faster with whole
-// pairs on its local layers (8-9 blocks a pair, 7.2 blocks a balanced share)
-// and 2.5x slower with them on its long global layers.  Whole pairs win when
-// waves x the longest pair stays within kWholeSlack blocks of the balanced
-// share.  Lengths come from the host copy when given, else from max_seq_len.
-constexpr int kWholeSlack = 6;
-
-bool tc_whole_pairs(const mqa_batch *bt, int window, int heads, int head_dim)
-{
-    const long long g = tc_max_ctas(head_dim, heads);
-    if (g <= 0 || bt->batch <= 0)
-        return false;
-    const long long groups = (heads + 31) / 32, pairs = (long long)bt->batch * groups;
-    long long nb = 0, maxb = 0;
-    if (bt->seq_lens_host != nullptr) {
-        for (int b = 0; b < bt->batch; ++b) {
-            const long long t = (tiles_for(bt->seq_lens_host[b], window) + 1) / 2;
-            nb += t;
-            maxb = t > maxb ? t : maxb;
-        }
-    } else {
-        maxb = (tiles_bound(bt->max_seq_len, window) + 1) / 2;
-        nb = maxb * bt->batch;
-    }
-    nb *= groups;
-    const long long ctas = g < nb ? g : nb;
-    if (ctas <= 0)
-        return true;
-    const long long waves = (pairs + g - 1) / g;
-    return waves * maxb * ctas <= nb + kWholeSlack * ctas;  // waves * maxb <= share + slack
-}
-
-int tc_auto_splits(int batch, int heads, int head_dim)
-{
-    const long long g = tc_max_ctas(head_dim, heads);
-    const long long pairs = (long long)batch * ((heads + 31) / 32);
-    long long s = (2 * g + pairs - 1) / pairs;
-    if (s < 2)
-        s = 2;
-    return (int)(s > MQA_MAX_SPLITS ? MQA_MAX_SPLITS : s);
 }
 
 // Upper bound of tiles_for(L, W) over 1 <= L <= Lmax.
@@ -224,64 +161,76 @@ int tiles_bound(int Lmax, int W)
     return win < all ? win : all;
 }
 
-struct Plan {
-    int max_tiles;
-    int tiles_per_split;
-    int num_splits;
-};
-
-int plan_decode(const mqa_batch *bt, int window, int heads, int head_dim, int requested, Plan *p)
+// Head groups of a (sequence): 32 query heads each at head_dim 128, 16 at head_dim 64.
+int head_groups(int32_t heads, int32_t head_dim)
 {
-    long long total = 0;
-    int max_tiles = 0;
+    const int g = decode_heads_per_group(head_dim);
+    return (heads + g - 1) / g;
+}
+
+// Key blocks of the decode kernel: 128 tokens (head_dim 128) or 256 (head_dim 64,
+// two tokens a row), i.e. 2 or 4 of the 64-token tiles.
+int blocks_of_tiles(int tiles, int head_dim)
+{
+    const int t = head_dim == 64 ? 4 : 2;
+    return (tiles + t - 1) / t;
+}
+
+// The balanced (persistent) decode: CTAs it runs at most (one per SM).
+int tc_max_ctas()
+{
+    const int sms = sm_count();
+    if (sms <= 0)
+        return 0;
+    const int g = sms * tc_ctas_per_sm();
+    return g < kTcMaxCtas ? g : kTcMaxCtas;
+}
+
+// Whether the automatic plan runs one CTA per (sequence, head group) instead of
+// balanced shares.  Cutting a pair between CTAs costs far more than its blocks
+// (the pieces' epilogues and reference moves, the merge kernel): measured on
+// GB300, a 24-layer step ran 17% faster with whole pairs on its local layers
+// (8-9 blocks a pair, 7.2 blocks a balanced share) and 2.5x slower with them on
+// its long global layers.  Whole pairs win when waves x the longest pair stays
+// within kWholeSlack blocks of the balanced share.  Lengths come from the host
+// copy when given, else from max_seq_len.
+constexpr int kWholeSlack = 6;
+
+bool tc_whole_pairs(const mqa_batch *bt, int window, int heads, int head_dim)
+{
+    const long long g = tc_max_ctas();
+    if (g <= 0 || bt->batch <= 0)
+        return false;
+    const long long groups = head_groups(heads, head_dim), pairs = (long long)bt->batch * groups;
+    long long nb = 0, maxb = 0;
     if (bt->seq_lens_host != nullptr) {
         for (int b = 0; b < bt->batch; ++b) {
-            const int t = tiles_for(bt->seq_lens_host[b], window);
-            total += t;
-            if (t > max_tiles)
-                max_tiles = t;
+            const long long t = blocks_of_tiles(tiles_for(bt->seq_lens_host[b], window), head_dim);
+            nb += t;
+            maxb = t > maxb ? t : maxb;
         }
     } else {
-        max_tiles = tiles_bound(bt->max_seq_len, window);
-        total = (long long)max_tiles * bt->batch;
+        maxb = blocks_of_tiles(tiles_bound(bt->max_seq_len, window), head_dim);
+        nb = maxb * bt->batch;
     }
-    int splits = requested;
-    if (splits == 0) {
-        // the most splits whose CTAs still fit in one wave of resident CTAs
-        // (a second, partial wave would pay every CTA's start-up latency twice)
-        const int sms = sm_count();
-        if (sms <= 0)
-            return MQA_ERR_CUDA;
-        const int groups = (heads + 31) / 32;
-        const long long slots = (long long)sms * ctas_per_sm(head_dim, heads);
-        splits = 1;
-        for (int s = 2; s <= max_tiles && s <= MQA_MAX_SPLITS; ++s) {
-            const int tps = (max_tiles + s - 1) / s;
-            if (tps < kMinTilesPerSplit)
-                break;
-            long long ctas = 0;
-            if (bt->seq_lens_host != nullptr) {
-                for (int b = 0; b < bt->batch; ++b)
-                    ctas += (tiles_for(bt->seq_lens_host[b], window) + tps - 1) / tps;
-            } else {
-                ctas = (long long)bt->batch * ((max_tiles + tps - 1) / tps);
-            }
-            ctas *= groups;
-            if (ctas > slots)
-                break;
-            splits = s;
-        }
-    }
-    if (splits < 1)
-        splits = 1;
-    if (splits > MQA_MAX_SPLITS)
-        splits = MQA_MAX_SPLITS;
-    if (splits > max_tiles)
-        splits = max_tiles;
-    p->max_tiles = max_tiles;
-    p->tiles_per_split = (max_tiles + splits - 1) / splits;
-    p->num_splits = (max_tiles + p->tiles_per_split - 1) / p->tiles_per_split;
-    return MQA_OK;
+    nb *= groups;
+    const long long ctas = g < nb ? g : nb;
+    if (ctas <= 0)
+        return true;
+    const long long waves = (pairs + g - 1) / g;
+    return waves * maxb * ctas <= nb + kWholeSlack * ctas;  // waves * maxb <= share + slack
+}
+
+// The split count whose workspace holds the partials of every resident CTA (two
+// slots of a head group's rows per CTA).
+int tc_auto_splits(int batch, int heads, int head_dim)
+{
+    const long long g = tc_max_ctas();
+    const long long pairs = (long long)batch * head_groups(heads, head_dim);
+    long long s = (2 * g + pairs - 1) / pairs;
+    if (s < 2)
+        s = 2;
+    return (int)(s > MQA_MAX_SPLITS ? MQA_MAX_SPLITS : s);
 }
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -291,12 +240,11 @@ size_t lse_offset(int32_t batch, int32_t heads, int32_t head_dim, int32_t splits
     return round256((size_t)batch * splits * heads * head_dim * sizeof(float));
 }
 
-size_t counters_offset(int32_t batch, int32_t heads, int32_t head_dim, int32_t splits)
+size_t descs_offset(int32_t batch, int32_t heads, int32_t head_dim, int32_t splits)
 {
     return round256(lse_offset(batch, heads, head_dim, splits) + (size_t)batch * splits * heads * sizeof(float));
 }
 
-int head_groups(int32_t heads) { return (heads + 31) / 32; }
 
 // A window-bounded cache (ring of R pages) serves only reads inside its resident
 // pages: the R most recent pages of a sequence hold any run of up to
@@ -374,10 +322,8 @@ size_t mqa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t hea
 {
     if (num_splits <= 1 || batch <= 0 || num_q_heads <= 0 || head_dim <= 0)
         return 0;
-    // last region: the warp-MMA kernel's tickets or the tcgen05 kernel's merge descriptors
-    const size_t tickets = (size_t)batch * head_groups(num_q_heads) * sizeof(int32_t);
-    const size_t descs = (size_t)2 * kTcMaxCtas * 8 * sizeof(int32_t);
-    return counters_offset(batch, num_q_heads, head_dim, num_splits) + (tickets > descs ? tickets : descs);
+    // partials, log-sum-exps, then the merge descriptors of up to kTcMaxCtas CTAs
+    return descs_offset(batch, num_q_heads, head_dim, num_splits) + (size_t)2 * kTcMaxCtas * 8 * sizeof(int32_t);
 }
 
 int mqa_decode_auto_splits(const mqa_batch *batch, int32_t window, int32_t num_q_heads, int32_t head_dim,
@@ -392,15 +338,9 @@ int mqa_decode_auto_splits(const mqa_batch *batch, int32_t window, int32_t num_q
         return rc;
     if (batch->batch == 0)
         return 1;
-    if (decode_uses_tc(head_dim, num_q_heads)) {
-        if (tc_max_ctas(head_dim, num_q_heads) <= 0)
-            return MQA_ERR_CUDA;
-        return tc_whole_pairs(batch, window, num_q_heads, head_dim) ? 1
-                                                                     : tc_auto_splits(batch->batch, num_q_heads, head_dim);
-    }
-    Plan p;
-    rc = plan_decode(batch, window, num_q_heads, head_dim, 0, &p);
-    return rc == MQA_OK ? p.num_splits : rc;
+    if (tc_max_ctas() <= 0)
+        return MQA_ERR_CUDA;
+    return tc_whole_pairs(batch, window, num_q_heads, head_dim) ? 1 : tc_auto_splits(batch->batch, num_q_heads, head_dim);
 }
 
 int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_t *layer_to_kv, int32_t num_layers,
@@ -426,67 +366,59 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
     if (q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out))
         return MQA_ERR_INVALID_ARG;
     const int D = cache->head_dim;
-    const bool tc = decode_uses_tc(D, num_q_heads);
-    Plan plan;
-    if (tc) {
-        // tensor-core kernel: num_splits 1 = one CTA per (sequence, head group);
-        // otherwise balanced shares over the CTAs whose partials fit the split
-        // count's workspace (the automatic count fits every resident CTA)
-        plan.max_tiles = 0;
-        plan.tiles_per_split = 0;
-        plan.num_splits = num_splits;
-        if (num_splits == 0)
-            plan.num_splits = tc_whole_pairs(batch, window, num_q_heads, D) ? 1
-                                                                            : tc_auto_splits(batch->batch, num_q_heads, D);
-        if (plan.num_splits > 1 && tc_max_ctas(D, num_q_heads) <= 0)
-            return MQA_ERR_CUDA;
-    } else {
-        rc = plan_decode(batch, window, num_q_heads, D, num_splits, &plan);
-        if (rc != MQA_OK)
-            return rc;
-    }
+    // num_splits 1 = one CTA per (sequence, head group); otherwise balanced shares
+    // over the CTAs whose partials fit the split count's workspace (the automatic
+    // count fits every resident CTA)
+    int splits = num_splits;
+    if (splits == 0)
+        splits = tc_whole_pairs(batch, window, num_q_heads, D) ? 1 : tc_auto_splits(batch->batch, num_q_heads, D);
     DecodeArgs a;
     std::memset(&a, 0, sizeof a);
-    if (plan.num_splits > 1) {
-        const size_t need = mqa_decode_workspace_size(batch->batch, num_q_heads, D, plan.num_splits);
+    const long long pairs = (long long)batch->batch * head_groups(num_q_heads, D);
+    if (splits > 1) {
+        const size_t need = mqa_decode_workspace_size(batch->batch, num_q_heads, D, splits);
         if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
             return MQA_ERR_WORKSPACE;
+        const long long g = tc_max_ctas();
+        if (g <= 0)
+            return MQA_ERR_CUDA;
+        // CTA c keeps its partials in rows [2c, 2c + 2) x (heads of a group) of head_dim
+        // floats (and as many log-sum-exps): the regions sized for `splits` hold
+        // batch x splits x heads rows, i.e. pairs x splits / 2 CTAs
         a.o_partial = static_cast<float *>(workspace);
         a.lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                          lse_offset(batch->batch, num_q_heads, D, plan.num_splits));
-        int32_t *last = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
-                                                    counters_offset(batch->batch, num_q_heads, D, plan.num_splits));
-        if (tc)
-            a.merge_desc = last;  // rewritten by every call: no zeroing
-        else if (plan.num_splits <= kMaxFusedSplits)
-            a.counters = last;
+                                          lse_offset(batch->batch, num_q_heads, D, splits));
+        a.merge_desc = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                                   descs_offset(batch->batch, num_q_heads, D, splits));
+        const long long fit = pairs * splits / 2;
+        a.persistent = 1;
+        a.persist_ctas = (int)(g < fit ? g : fit);
+    } else {
+        if (pairs > INT32_MAX)
+            return MQA_ERR_INVALID_ARG;
+        a.persistent = 0;
+        a.persist_ctas = (int)pairs;
     }
-    if (tc) {
-        const long long pairs = (long long)batch->batch * head_groups(num_q_heads);
-        if (plan.num_splits > 1) {
-            long long g = tc_max_ctas(D, num_q_heads);
-            const long long fit = pairs * plan.num_splits / 2;  // CTAs whose 2 partial slots fit
-            a.persistent = 1;
-            a.persist_ctas = (int)(g < fit ? g : fit);
-        } else {
-            if (pairs > INT32_MAX)
-                return MQA_ERR_INVALID_ARG;
-            a.persistent = 0;
-            a.persist_ctas = (int)pairs;
+    if (D == 64) {
+        // two tokens a row: the codes as [num_blocks * page_size / 2][128], 8-row boxes (16 tokens)
+        if ((rc = make_code_map(&a.k_map, cache->k_codes, cache->num_blocks, cache->page_size / 2, 128, 8)) != MQA_OK)
+            return rc;
+        if ((rc = make_code_map(&a.v_map, cache->v_codes, cache->num_blocks, cache->page_size / 2, 128, 8)) != MQA_OK)
+            return rc;
+    } else {
+        if ((rc = make_code_map(&a.k_map, cache->k_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
+            return rc;
+        if ((rc = make_code_map(&a.v_map, cache->v_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
+            return rc;
+        if (cache->page_size == kTileTokens) {
+            // whole 64-token tiles (= pages) in one copy per tensor
+            if ((rc = make_code_map(&a.k_map64, cache->k_codes, cache->num_blocks, cache->page_size, D,
+                                    kTileTokens)) != MQA_OK)
+                return rc;
+            if ((rc = make_code_map(&a.v_map64, cache->v_codes, cache->num_blocks, cache->page_size, D,
+                                    kTileTokens)) != MQA_OK)
+                return rc;
         }
-    }
-    if ((rc = make_code_map(&a.k_map, cache->k_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
-        return rc;
-    if ((rc = make_code_map(&a.v_map, cache->v_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
-        return rc;
-    if (tc && cache->page_size == kTileTokens) {
-        // whole 64-token tiles (= pages) in one copy per tensor
-        if ((rc = make_code_map(&a.k_map64, cache->k_codes, cache->num_blocks, cache->page_size, D, kTileTokens)) !=
-            MQA_OK)
-            return rc;
-        if ((rc = make_code_map(&a.v_map64, cache->v_codes, cache->num_blocks, cache->page_size, D, kTileTokens)) !=
-            MQA_OK)
-            return rc;
     }
     a.k_scale = cache->k_scale;
     a.v_scale = cache->v_scale;
@@ -503,22 +435,8 @@ int mqa_decode_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_
     a.ring = batch->ring_blocks;
     a.num_q_heads = num_q_heads;
     a.window = window;
-    a.tiles_per_split = plan.tiles_per_split;
-    a.num_splits = plan.num_splits;
     a.q_scale_log2 = sm_scale * 1.4426950408889634f;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // up to kMaxFusedSplits splits the decode kernel merges them itself (its
-    // tickets start at zero); wider splits go through the combine kernel
-    if (a.counters != nullptr &&
-        cudaMemsetAsync(a.counters, 0, (size_t)a.batch * head_groups(num_q_heads) * sizeof(int32_t), s) !=
-            cudaSuccess)
-        return MQA_ERR_CUDA;
-    if (launch_decode(a, D, s) != cudaSuccess)
-        return MQA_ERR_CUDA;
-    if (!tc && plan.num_splits > 1 && a.counters == nullptr &&
-        launch_combine(a.o_partial, a.lse, a.batch, a.num_splits, num_q_heads, D, a.out, s) != cudaSuccess)
-        return MQA_ERR_CUDA;
-    return MQA_OK;
+    return launch_decode_tc(a, D, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
 }
 
 int split_kv_combine(const float *o_partial, const float *lse, int32_t batch, int32_t num_splits,

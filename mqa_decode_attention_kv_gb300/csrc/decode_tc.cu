@@ -71,8 +71,9 @@ namespace {
 struct TcCfg {
     static constexpr int D = 128;
     static constexpr int NH = 32;                    // heads per group (MMA N)
-    static constexpr int BT = 128;                   // tokens per block (M of S^T, K of O^T)
-    static constexpr int BOXES = BT / kChunkTokens;  // 8 TMA boxes of 16 tokens
+    static constexpr int BT = 128;                   // rows per block (M of S^T, K of O^T)
+    static constexpr int SCL_TOK = 2 * BT;           // token scales per stage and tensor (up to 256 tokens)
+    static constexpr int BOXES = SCL_TOK / kChunkTokens;  // box flags per stage (16 tokens a box)
     static constexpr int NW = 2;                     // worker warpgroups
     static constexpr int RING = 5;                   // ring stages (codes in flight, then fp16 V)
     // a control warpgroup after the workers: the MMA warp, the TMA warp and two idle warps
@@ -88,10 +89,11 @@ struct TcCfg {
     // shared memory (offsets from a 1024-aligned base)
     static constexpr int OFF_RING = 0;
     static constexpr int OFF_QH = OFF_RING + RING * STAGE;     // [2 slots] fp16 Q [32 h][128 d], core layout
-    static constexpr int OFF_QRAW = OFF_QH + 2 * NH * D * 2;   // bf16 Q [32 h][128 d] as copied (next piece)
+    static constexpr int QH_SLOT = NH * D * 2;                 // one slot of fp16 Q
+    static constexpr int OFF_QRAW = OFF_QH + 2 * QH_SLOT;      // bf16 Q [<= 32 h][<= 128 d] as copied (next piece)
     static constexpr int OFF_PH = OFF_QRAW + NH * D * 2;       // [NW] fp16 P' [128 tok][32 h], core layout
-    static constexpr int OFF_SCL = OFF_PH + NW * BT * NH * 2;  // [RING][2][128] fp32 K, V token scales (TMA)
-    static constexpr int OFF_OK = OFF_SCL + RING * 2 * BT * 4;  // [RING][8] box arrived
+    static constexpr int OFF_SCL = OFF_PH + NW * BT * NH * 2;  // [RING][2][SCL_TOK] fp32 K, V token scales (TMA)
+    static constexpr int OFF_OK = OFF_SCL + RING * 2 * SCL_TOK * 4;  // [RING][BOXES] box arrived
     // per worker group: red [4 warps][32], vred [4], mref [32], fac [NW][32]
     static constexpr int WG_RED = 0, WG_VRED = 512, WG_MREF = 528, WG_FAC = 656;
     static constexpr int WG_BYTES = (WG_FAC + NW * NH * 4 + 15) / 16 * 16;
@@ -137,6 +139,28 @@ static_assert(TcCfg::OFF_QRAW % 16 == 0 && TcCfg::OFF_SCL % 16 == 0 && TcCfg::OF
               "16-byte alignment");
 static_assert(TcCfg::K_COL + TcCfg::NW * 64 <= TcCfg::TMEM_COLS, "tensor memory budget");
 
+// The two row formats of a key block (128 rows of 128 code bytes = tensor-memory lanes):
+// head_dim 128, a row is one token; head_dim 64, a row is two consecutive tokens (the
+// cache's bytes as they lie: the second token's codes are columns 64-127).  With pairs
+// the 32 MMA columns are (token of the row, head): columns 0-15 hold heads 0-15 of
+// the row's first token, columns 16-31 the same heads of its second; the B operand Q
+// of S^T = K Q^T holds head h's query in columns 0-63 of column h and 64-127 of column
+// h + 16 (zeros elsewhere), so each column scores one token, and O^T += V^T P' leaves
+// the first token's sums in rows 0-63 of columns 0-15 and the second's in rows 64-127
+// of columns 16-31 (the other quadrants are discarded).  Each column keeps its own
+// softmax state; the epilogue merges the two columns of a head.  Groups with fewer
+// heads than columns (8 or 16 query heads) leave the rest of their columns at a zero
+// query, computed and discarded.
+template <bool PAIR>
+struct TcMode {
+    static constexpr int TPR = PAIR ? 2 : 1;                        // tokens per row
+    static constexpr int DH = TcCfg::D / TPR;                       // head_dim
+    static constexpr int NHG = TcCfg::NH / TPR;                     // query heads per group
+    static constexpr int TILES = 2 * TPR;                           // 64-token tiles per block
+    static constexpr int BOXES = TcCfg::BT * TPR / kChunkTokens;    // 16-token boxes per block
+    static_assert(BOXES <= TcCfg::BOXES && TcCfg::BT * TPR <= TcCfg::SCL_TOK, "stage flags and scales");
+};
+
 // Reduce 32 per-head values over the 32 lanes of a warp with 31 shuffles (a
 // butterfly that halves the values each lane keeps at every step): lane L
 // returns the reduction of head L.  v is consumed.
@@ -158,8 +182,9 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
 }
 
 // Key blocks of a sequence of length L: the 64-token tiles from the one
-// holding the window start to the one holding L-1, paired into 128-token
-// blocks (the last block may hold a single tile).  0 for an invalid length.
+// holding the window start to the one holding L-1, grouped TILES to a block
+// (the last block may hold fewer).  0 for an invalid length.
+template <int TILES>
 __device__ __forceinline__ int seq_blocks(int L, int window, int max_seq_len, int &t_first, int &lo)
 {
     t_first = 0;
@@ -169,7 +194,7 @@ __device__ __forceinline__ int seq_blocks(int L, int window, int max_seq_len, in
     lo = (window > 0 && L > window) ? L - window : 0;
     t_first = lo / kTileTokens;
     const int t_last = (L - 1) / kTileTokens;
-    return (t_last - t_first + 2) >> 1;
+    return (t_last - t_first + TILES) / TILES;
 }
 
 // Position in the (sequence, head group, block) list.
@@ -180,11 +205,12 @@ struct Cursor {
 };
 
 // Load sequence b's shape into the cursor; then skip sequences without blocks.
+template <int TILES>
 __device__ __forceinline__ void cursor_seek(Cursor &c, const DecodeArgs &a)
 {
     while (c.b < a.batch) {
         c.L = __ldg(a.seq_lens + c.b);
-        c.nblk = seq_blocks(c.L, a.window, a.max_seq_len, c.t_first, c.lo);
+        c.nblk = seq_blocks<TILES>(c.L, a.window, a.max_seq_len, c.t_first, c.lo);
         if (c.nblk > 0)
             return;
         ++c.b;
@@ -193,6 +219,7 @@ __device__ __forceinline__ void cursor_seek(Cursor &c, const DecodeArgs &a)
     }
 }
 
+template <int TILES>
 __device__ __forceinline__ void cursor_next(Cursor &c, const DecodeArgs &a, int groups)
 {
     if (++c.blk < c.nblk)
@@ -202,7 +229,7 @@ __device__ __forceinline__ void cursor_next(Cursor &c, const DecodeArgs &a, int 
         return;
     c.g = 0;
     ++c.b;
-    cursor_seek(c, a);
+    cursor_seek<TILES>(c, a);
 }
 
 // The CTA whose share holds list entry x (the largest c with floor(c*N/G) <= x).
@@ -224,10 +251,11 @@ __device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t w, uint32_t &lo,
 }
 
 // Partial-output row of piece s (0 = the pair's first piece, in CTA c_lo) of a
-// merged pair: CTA c_lo + s, slot slot_lo for s == 0 else 0, head jh.
-__device__ __forceinline__ size_t merge_row(int c_lo, int s, int slot_lo, int jh)
+// merged pair: CTA c_lo + s, slot slot_lo for s == 0 else 0, head jh; a slot
+// holds hs rows (the heads of a group that exist).
+__device__ __forceinline__ size_t merge_row(int c_lo, int s, int slot_lo, int jh, int hs)
 {
-    return (size_t)(2 * (c_lo + s) + (s == 0 ? slot_lo : 0)) * TcCfg::NH + jh;
+    return (size_t)(2 * (c_lo + s) + (s == 0 ? slot_lo : 0)) * hs + jh;
 }
 
 // Whether worker group w computes a block of the piece whose blocks are list
@@ -248,17 +276,21 @@ __device__ __forceinline__ void regs_dec()
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(TcCfg::REG_CTRL));
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __grid_constant__ DecodeArgs a)
 {
     using C = TcCfg;
+    using MD = TcMode<PAIR>;
+    // D, NH: a row's code bytes and the MMA columns; DH, NHG: head_dim and query heads per group
     constexpr int D = C::D, NH = C::NH, RING = C::RING, BT = C::BT, NW = C::NW;
+    constexpr int DH = MD::DH, NHG = MD::NHG, TPR = MD::TPR, TILES = MD::TILES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *qh = base + C::OFF_QH;
     uint8_t *qraw = base + C::OFF_QRAW;
     uint8_t *ph = base + C::OFF_PH;
     uint32_t *box_ok = reinterpret_cast<uint32_t *>(base + C::OFF_OK);
-    float *scl = reinterpret_cast<float *>(base + C::OFF_SCL);  // [RING][2][128] token scales, with the codes
+    float *scl = reinterpret_cast<float *>(base + C::OFF_SCL);  // [RING][2][SCL_TOK] token scales, with the codes
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 4);
     volatile int *q_issued = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 8);  // raw Q copies issued
@@ -279,7 +311,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     static_assert(3 * C::RING + 5 * C::NW + 7 == C::NBAR, "barrier count");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int groups = (a.num_q_heads + NH - 1) / NH;
+    const int groups = (a.num_q_heads + NHG - 1) / NHG;
+    const int HS = min(a.num_q_heads, NHG);  // partial-output rows per slot: the heads of a group
     const int G = gridDim.x;
     const int cta = blockIdx.x;
     const bool balanced = a.persistent != 0;
@@ -310,7 +343,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     if (warp == C::MMA_WARP)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
     if (warp == C::TMA_WARP && lane == 0) {
-        const bool p64 = a.page_size == kTileTokens;
+        const bool p64 = !PAIR && a.page_size == kTileTokens;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.k_map64 : &a.k_map))
                      : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.v_map64 : &a.v_map))
@@ -326,8 +359,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             const char *row = reinterpret_cast<const char *>(a.block_table + (size_t)bb * a.max_blocks);
             for (int off = lane * 128; off < a.max_blocks * 4 && off < 64 * 128; off += 32 * 128)
                 prefetch_l2(row + off);
-            const char *qp = reinterpret_cast<const char *>(a.q + ((size_t)bb * a.num_q_heads + gg * NH) * D);
-            for (int off = lane * 128; off < NH * D * 2; off += 32 * 128)
+            const char *qp = reinterpret_cast<const char *>(a.q + ((size_t)bb * a.num_q_heads + gg * NHG) * DH);
+            for (int off = lane * 128; off < min(NHG, a.num_q_heads - gg * NHG) * DH * 2; off += 32 * 128)
                 prefetch_l2(qp + off);
         }
     }
@@ -341,11 +374,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         int nb = 0;
         if (tid < a.batch) {
             int tf, lo;
-            nb = seq_blocks(__ldg(a.seq_lens + tid), a.window, a.max_seq_len, tf, lo);
+            nb = seq_blocks<TILES>(__ldg(a.seq_lens + tid), a.window, a.max_seq_len, tf, lo);
             if (nb == 0 && tid % G == cta) {
                 set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);
-                uint4 *dst = reinterpret_cast<uint4 *>(a.out + (size_t)tid * a.num_q_heads * D);
-                for (int k = 0; k < a.num_q_heads * D / 8; ++k)
+                uint4 *dst = reinterpret_cast<uint4 *>(a.out + (size_t)tid * a.num_q_heads * DH);
+                for (int k = 0; k < a.num_q_heads * DH / 8; ++k)
                     dst[k] = make_uint4(0, 0, 0, 0);
             }
         }
@@ -389,12 +422,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         for (int bb = tid; bb < a.batch; bb += C::THREADS) {
             int tf, lo;
             const int L = __ldg(a.seq_lens + bb);
-            const int nb = seq_blocks(L, a.window, a.max_seq_len, tf, lo);
+            const int nb = seq_blocks<TILES>(L, a.window, a.max_seq_len, tf, lo);
             mine += nb;
             if (nb == 0 && bb % G == cta) {
                 set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);
-                uint4 *dst = reinterpret_cast<uint4 *>(a.out + (size_t)bb * a.num_q_heads * D);
-                for (int k = 0; k < a.num_q_heads * D / 8; ++k)
+                uint4 *dst = reinterpret_cast<uint4 *>(a.out + (size_t)bb * a.num_q_heads * DH);
+                for (int k = 0; k < a.num_q_heads * DH / 8; ++k)
                     dst[k] = make_uint4(0, 0, 0, 0);
             }
         }
@@ -426,7 +459,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
             const int bb = b0 + tid;
             int tf, lo, nb = 0;
             if (bb < a.batch)
-                nb = seq_blocks(__ldg(a.seq_lens + bb), a.window, a.max_seq_len, tf, lo);
+                nb = seq_blocks<TILES>(__ldg(a.seq_lens + bb), a.window, a.max_seq_len, tf, lo);
             int x = nb;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -460,7 +493,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         if (tid == 0) {
             const int bb = cta / groups, gg = cta % groups;
             int tf, lo;
-            const int nb = seq_blocks(__ldg(a.seq_lens + bb), a.window, a.max_seq_len, tf, lo);
+            const int nb = seq_blocks<TILES>(__ldg(a.seq_lens + bb), a.window, a.max_seq_len, tf, lo);
             start_pos[0] = bb;
             start_pos[1] = gg;
             start_pos[2] = 0;
@@ -474,10 +507,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         __syncthreads();
         if (start_pos[3] == 0) {
             const int bb = cta / groups, gg = cta % groups;
-            for (int r = tid; r < NH * D / 8; r += C::THREADS) {
-                const int h = gg * NH + r / (D / 8);
+            for (int r = tid; r < NHG * DH / 8; r += C::THREADS) {
+                const int h = gg * NHG + r / (DH / 8);
                 if (h < a.num_q_heads)
-                    reinterpret_cast<uint4 *>(a.out + ((size_t)bb * a.num_q_heads + h) * D)[r % (D / 8)] =
+                    reinterpret_cast<uint4 *>(a.out + ((size_t)bb * a.num_q_heads + h) * DH)[r % (DH / 8)] =
                         make_uint4(0, 0, 0, 0);
             }
         }
@@ -503,7 +536,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     c0.b = start_pos[0];
     c0.g = start_pos[1];
     c0.blk = start_pos[2];
-    cursor_seek(c0, a);  // loads the shape of sequence c0.b (which has blocks)
+    cursor_seek<TILES>(c0, a);  // loads the shape of sequence c0.b (which has blocks)
     // registers: the control warpgroup gives most of its share to the worker groups
     if (warp < 4 * NW)
         regs_inc();
@@ -513,7 +546,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
     if (warp < 4 * NW) {
         // ================================================================ worker groups
         const int w = warp >> 2, wj = warp & 3;
-        const int tok = 32 * wj + lane;                        // token row of every block = tensor-memory lane
+        const int tok = 32 * wj + lane;                        // row of every block = tensor-memory lane
         const uint32_t lane_base = (uint32_t)(32 * wj) << 16;  // this warp's tensor-memory lanes
         const int BAR_WG = 1 + w;                              // named barrier of this group
         uint8_t *wg = base + C::OFF_WG + w * C::WG_BYTES;
@@ -524,10 +557,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         uint8_t *pw = ph + w * BT * NH * 2;                        // this group's P'
         const uint32_t s_col = C::S_COL + (uint32_t)w * NH, k_col = C::K_COL + (uint32_t)w * 64;
         if (w == 0 && wj == 0 && lane == 0) {
-            // the first piece's Q (bf16, 32 heads x 256 B, contiguous): group 0 converts it
+            // the first piece's Q (bf16, the group's heads x head_dim, contiguous): group 0 converts it
+            const uint32_t qb = (uint32_t)min(NHG, a.num_q_heads - c0.g * NHG) * DH * 2;
             *q_issued = 1;
-            mbar_arrive_expect_tx(qfull, NH * D * 2);
-            bulk_load(qraw, a.q + ((size_t)c0.b * a.num_q_heads + c0.g * NH) * D, NH * D * 2, qfull);
+            mbar_arrive_expect_tx(qfull, qb);
+            bulk_load(qraw, a.q + ((size_t)c0.b * a.num_q_heads + c0.g * NHG) * DH, qb, qfull);
         }
         Cursor cur = c0;
         float l_acc[NH];  // this token's sum of p per head, for the current piece
@@ -554,20 +588,25 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 uint8_t *slot = base + C::OFF_SLOT + s * C::SLOT_BYTES;
                 if (mine) {
                     // ---- this group converts the piece's Q into slot s (free once piece-2's
-                    // epilogue read it) and sums it per head; lane = head
+                    // epilogue read it) and sums it per column; lane = column, whose head is
+                    // lane % NHG (heads past the group's last read as zero)
                     if (piece >= 2)
                         ok &= wait_phase(sfree + s, (uint32_t)((piece - 2) >> 1) & 1u, abort_flag);
                     ok &= wait_phase(qfull, (uint32_t)piece & 1u, abort_flag);
-                    const uint8_t *qrow = qraw + lane * D * 2;
+                    const int hc = lane % NHG;
+                    const bool hreal = hc < min(NHG, a.num_q_heads - cur.g * NHG);
+                    const uint8_t *qrow = qraw + hc * DH * 2;
                     float m = 0.f;
+                    if (hreal) {
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * ((k + lane) & 15));
-                        const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+                        for (int k = 0; k < DH / 8; ++k) {
+                            const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * ((k + lane) & (DH / 8 - 1)));
+                            const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[t] << 16)),
-                                               fabsf(__uint_as_float(w4[t] & 0xffff0000u))));
+                            for (int t = 0; t < 4; ++t)
+                                m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[t] << 16)),
+                                                   fabsf(__uint_as_float(w4[t] & 0xffff0000u))));
+                        }
                     }
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1)
@@ -579,11 +618,15 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                         e = min(120, max(-120, 14 - x));
                     }
                     const float f = exp2i(e);
-                    float qsum = 0.f;  // this warp's d range of head `lane`, as the tensor core sees it
+                    float qsum = 0.f;  // this warp's range of column `lane`, as the tensor core sees it
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const int c = 4 * wj + ((t + lane) & 3);  // 8-d chunk: d = 8c .. 8c+7
-                        const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + 16 * c);
+                        const int c = 4 * wj + ((t + lane) & 3);  // 8-wide chunk of the row: 8c .. 8c+7
+                        // with pairs, chunks 0-7 face a row's first token, 8-15 its second
+                        const bool live = hreal && (!PAIR || (c >> 3) == lane / NHG);
+                        uint4 qv = make_uint4(0u, 0u, 0u, 0u);
+                        if (live)
+                            qv = *reinterpret_cast<const uint4 *>(qrow + 16 * (c % (DH / 8)));
                         const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
                         uint32_t hv[4];
 #pragma unroll
@@ -594,7 +637,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                             qsum += __low2float(h2);
                             qsum += __high2float(h2);
                         }
-                        *reinterpret_cast<uint4 *>(qh + s * NH * D * 2 + core_off(lane, 8 * c, C::Q_SR, C::Q_SC)) =
+                        *reinterpret_cast<uint4 *>(qh + s * C::QH_SLOT + core_off(lane, 8 * c, C::Q_SR, C::Q_SC)) =
                             make_uint4(hv[0], hv[1], hv[2], hv[3]);
                     }
                     red[wj * NH + lane] = qsum;
@@ -610,10 +653,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                         if (lane == 0 && i_next < n && ok && !*abort_flag) {
                             Cursor nx = cur;
                             nx.blk = cur.nblk - 1;
-                            cursor_next(nx, a, groups);
+                            cursor_next<TILES>(nx, a, groups);
+                            const uint32_t qb = (uint32_t)min(NHG, a.num_q_heads - nx.g * NHG) * DH * 2;
                             *q_issued = *q_issued + 1;  // before the arrival that publishes it
-                            mbar_arrive_expect_tx(qfull, NH * D * 2);
-                            bulk_load(qraw, a.q + ((size_t)nx.b * a.num_q_heads + nx.g * NH) * D, NH * D * 2, qfull);
+                            mbar_arrive_expect_tx(qfull, qb);
+                            bulk_load(qraw, a.q + ((size_t)nx.b * a.num_q_heads + nx.g * NHG) * DH, qb, qfull);
                         }
                     }
                     named_bar(BAR_WG, 128);  // red reuse; the slot's bias and factor written
@@ -634,12 +678,16 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 uint8_t *st = base + C::OFF_RING + r * C::STAGE;
                 ok &= wait_phase(tfull + 2 * r + (wj >> 1), (uint32_t)(i / RING) & 1u, abort_flag);
                 tc_fence_after();
-                const uint8_t *crow = st + tok * D;  // this token's codes (K, then V at + CODES)
-                const int pos = (cur.t_first + 2 * cur.blk) * kTileTokens + tok;
-                const bool fetched = box_ok[r * C::BOXES + (tok >> 4)] != 0;
-                const bool valid = fetched && pos >= cur.lo && pos < cur.L;
-                const float ksv = fetched ? scl[r * 2 * BT + tok] : 0.f;
-                const float vsv = fetched ? scl[r * 2 * BT + BT + tok] : 0.f;
+                const uint8_t *crow = st + tok * D;  // this row's codes (K, then V at + CODES)
+                // the row's token(s): pos0 (and pos0 + 1 with pairs), in one box
+                const int pos0 = (cur.t_first + TILES * cur.blk) * kTileTokens + TPR * tok;
+                const bool fetched = box_ok[r * C::BOXES + ((TPR * tok) >> 4)] != 0;
+                const bool valid0 = fetched && pos0 >= cur.lo && pos0 < cur.L;
+                const bool valid1 = PAIR && fetched && pos0 + 1 >= cur.lo && pos0 + 1 < cur.L;
+                const float *sct = scl + r * 2 * C::SCL_TOK + TPR * tok;
+                const float ksv0 = fetched ? sct[0] : 0.f, vsv0 = fetched ? sct[C::SCL_TOK] : 0.f;
+                const float ksv1 = PAIR && fetched ? sct[1] : 0.f;
+                const float vsv1 = PAIR && fetched ? sct[C::SCL_TOK + 1] : 0.f;
                 // ---- K: 128 codes -> fp16 pairs in tensor memory (lane tok, 64 columns); the
                 // group's K buffer was last read by S^T of its previous block, which it waited for.
                 // (A loop, not unrolled: the kernel's instruction footprint is a bottleneck of its own.)
@@ -697,18 +745,20 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(vready + w);
-                // ---- scores of this token: S^T(i) row tok, 32 heads
+                // ---- scores of this row: S^T(i) row tok, 32 columns
                 ok &= wait_phase(sfull + w, (uint32_t)pj, abort_flag);
                 tc_fence_after();
                 uint32_t sr[NH];
                 tmem_ld32(tmem + lane_base + s_col, sr);
                 tmem_wait_ld();
-                const float kg = ksv * gh;  // raw score -> log2 domain
+                // raw score -> log2 domain; with pairs columns 16-31 score the row's second token
+                const float kg0 = ksv0 * gh, kg1 = ksv1 * gh;
                 float x[NH];
-                float dmax = -INFINITY;
+                float dmax0 = -INFINITY, dmax1 = -INFINITY;
 #pragma unroll
                 for (int q = 0; q < NH / 4; ++q) {
                     const float4 b4 = reinterpret_cast<const float4 *>(bias)[q];
+                    const float kg = (PAIR && q >= NH / 8) ? kg1 : kg0;
                     x[4 * q] = (__uint_as_float(sr[4 * q]) - b4.x) * kg;
                     x[4 * q + 1] = (__uint_as_float(sr[4 * q + 1]) - b4.y) * kg;
                     x[4 * q + 2] = (__uint_as_float(sr[4 * q + 2]) - b4.z) * kg;
@@ -717,11 +767,16 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
 #pragma unroll
                 for (int q = 0; q < NH / 4; ++q) {
                     const float4 m4 = reinterpret_cast<const float4 *>(mref)[q];
-                    dmax = fmaxf(dmax, fmaxf(fmaxf(x[4 * q] - m4.x, x[4 * q + 1] - m4.y),
-                                             fmaxf(x[4 * q + 2] - m4.z, x[4 * q + 3] - m4.w)));
+                    const float dq = fmaxf(fmaxf(x[4 * q] - m4.x, x[4 * q + 1] - m4.y),
+                                           fmaxf(x[4 * q + 2] - m4.z, x[4 * q + 3] - m4.w));
+                    if (PAIR && q >= NH / 8)
+                        dmax1 = fmaxf(dmax1, dq);
+                    else
+                        dmax0 = fmaxf(dmax0, dq);
                 }
                 // a group's first block of a piece always moves the references (they start at -inf)
-                const bool need = !took || (valid && (!(dmax <= 8.f) || !(vsv <= exp2i(E_run))));
+                const bool need = !took || (valid0 && (!(dmax0 <= 8.f) || !(vsv0 <= exp2i(E_run)))) ||
+                                  (valid1 && (!(dmax1 <= 8.f) || !(vsv1 <= exp2i(E_run))));
                 ok &= *abort_flag == 0;
                 if (named_bar_or(BAR_WG, 128, need || !ok)) {
                     if (named_bar_or(BAR_WG, 128, !ok))
@@ -731,10 +786,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                         float mv[NH];
 #pragma unroll
                         for (int h = 0; h < NH; ++h)
-                            mv[h] = valid ? x[h] : -INFINITY;
+                            mv[h] = ((PAIR && h >= NH / 2) ? valid1 : valid0) ? x[h] : -INFINITY;
                         red[wj * NH + lane] = warp_transpose_reduce<true>(mv, lane);  // head lane's warp max
                     }
-                    float vm = valid ? vsv : 0.f;
+                    float vm = fmaxf(valid0 ? vsv0 : 0.f, valid1 ? vsv1 : 0.f);
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1)
                         vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
@@ -755,7 +810,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     const float escale = took ? exp2i(max(E_run - E_new, -126)) : 1.f;
                     if (took) {
                         // this group's O of the piece (its previous O^T update is done, waited
-                        // above): row d = tok, 32 heads
+                        // above): row tok, 32 columns
                         const uint32_t o_col = C::O_COL + (uint32_t)(w * 2 + (piece & 1)) * NH;
                         uint32_t orr[NH];
                         tmem_ld32(tmem + lane_base + o_col, orr);
@@ -784,9 +839,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 }
                 took = true;
                 // ---- P' = 2^(score - ref) * s_v * 2^(6-E) as fp16: row tok of this group's P'
-                const float vf = valid ? vsv * exp2i(6 - E_run) : 0.f;
+                const float ef = exp2i(6 - E_run);
+                const float vf0 = valid0 ? vsv0 * ef : 0.f, vf1 = valid1 ? vsv1 * ef : 0.f;
 #pragma unroll
                 for (int q = 0; q < NH / 8; ++q) {
+                    const bool valid = (PAIR && q >= NH / 16) ? valid1 : valid0;
+                    const float vf = (PAIR && q >= NH / 16) ? vf1 : vf0;
                     const float4 ma = reinterpret_cast<const float4 *>(mref)[2 * q];
                     const float4 mb = reinterpret_cast<const float4 *>(mref)[2 * q + 1];
                     const float mq[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
@@ -844,7 +902,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     const bool whole_pair = piece_from_start && cur.blk == cur.nblk - 1;
                     const int oslot = piece_i0 == 0 ? 0 : 1;
                     if (wj == 0) {
-                        // head lane: the merged reference, sum, and every group's output factor
+                        // column lane: the merged reference, sum, and every group's output factor
                         const int h = lane;
                         float M = -INFINITY;
 #pragma unroll
@@ -863,19 +921,29 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                                 Ls += wu[u] * gs[NH + h];
                             }
                         }
+                        // with pairs, columns h and h ^ 16 are one head (a row's two tokens):
+                        // their reference Mt and sum Lt are shared, sh weighs this column's part
+                        float Mt = M, Lt = Ls, sh = 1.f;
+                        if (PAIR) {
+                            const float Mo = __shfl_xor_sync(0xffffffffu, M, 16);
+                            const float Lo = __shfl_xor_sync(0xffffffffu, Ls, 16);
+                            Mt = fmaxf(M, Mo);
+                            sh = M == -INFINITY ? 0.f : fast_exp2(M - Mt);
+                            Lt = Ls * sh + (Mo == -INFINITY ? 0.f : Lo * fast_exp2(Mo - Mt));
+                        }
 #pragma unroll
                         for (int u = 0; u < NW; ++u) {
                             float f = 0.f;
-                            if (Ls > 0.f && wu[u] > 0.f) {
+                            if (Lt > 0.f && wu[u] > 0.f) {
                                 const int Eu =
                                     reinterpret_cast<const int *>(slot + C::SL_GRP + u * C::SL_GRP_BYTES)[2 * NH];
-                                f = __fdividef(wu[u] * exp2i(Eu - 6), Ls);
+                                f = __fdividef(wu[u] * sh * exp2i(Eu - 6), Lt);
                             }
                             fac[u * NH + h] = f;
                         }
-                        if (!whole_pair && cur.g * NH + h < a.num_q_heads)
-                            a.lse[(size_t)(2 * cta + oslot) * NH + h] =
-                                Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+                        if (!whole_pair && h < NHG && cur.g * NHG + h < a.num_q_heads)
+                            a.lse[(size_t)(2 * cta + oslot) * HS + h] =
+                                Lt > 0.f ? (Mt + __log2f(Lt)) * 0.69314718055994531f : -INFINITY;
                     }
                     named_bar(BAR_WG, 128);
                     float acc[NH];
@@ -902,18 +970,45 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(sfree + s);  // slot s and the groups' O buffers s are free
-                    const int nh = min(NH, a.num_q_heads - cur.g * NH);  // heads of this group that exist
-                    if (whole_pair) {
-                        __nv_bfloat16 *dst = a.out + ((size_t)cur.b * a.num_q_heads + cur.g * NH) * D + tok;
+                    const int nh = min(NHG, a.num_q_heads - cur.g * NHG);  // heads of this group that exist
+                    if (PAIR) {
+                        // a head's two columns meet: row d + 64 (the second tokens' sums, columns
+                        // 16-31) hands them to row d through this group's P' buffer (free: the
+                        // group's last O^T update of the piece has completed)
+                        float *xb = reinterpret_cast<float *>(pw);  // [64 d][16 heads]
+                        if (tok >= DH) {
 #pragma unroll
-                        for (int h = 0; h < NH; ++h)
-                            if (h < nh)
-                                dst[(size_t)h * D] = __float2bfloat16_rn(acc[h]);
-                    } else {
-                        float *dst = a.o_partial + ((size_t)(2 * cta + oslot) * NH) * D + tok;
+                            for (int q = 0; q < NHG / 4; ++q)
+                                reinterpret_cast<float4 *>(xb + (tok - DH) * NHG)[q] =
+                                    make_float4(acc[NHG + 4 * q], acc[NHG + 4 * q + 1], acc[NHG + 4 * q + 2],
+                                                acc[NHG + 4 * q + 3]);
+                        }
+                        named_bar(BAR_WG, 128);
+                        if (tok < DH) {
 #pragma unroll
-                        for (int h = 0; h < NH; ++h)
-                            dst[(size_t)h * D] = acc[h];
+                            for (int q = 0; q < NHG / 4; ++q) {
+                                const float4 o4 = reinterpret_cast<const float4 *>(xb + tok * NHG)[q];
+                                acc[4 * q] += o4.x;
+                                acc[4 * q + 1] += o4.y;
+                                acc[4 * q + 2] += o4.z;
+                                acc[4 * q + 3] += o4.w;
+                            }
+                        }
+                    }
+                    if (tok < DH) {
+                        if (whole_pair) {
+                            __nv_bfloat16 *dst = a.out + ((size_t)cur.b * a.num_q_heads + cur.g * NHG) * DH + tok;
+#pragma unroll
+                            for (int h = 0; h < NHG; ++h)
+                                if (h < nh)
+                                    dst[(size_t)h * DH] = __float2bfloat16_rn(acc[h]);
+                        } else {
+                            float *dst = a.o_partial + ((size_t)(2 * cta + oslot) * HS) * DH + tok;
+#pragma unroll
+                            for (int h = 0; h < NHG; ++h)
+                                if (h < nh)
+                                    dst[(size_t)h * DH] = acc[h];
+                        }
                     }
                     if (!whole_pair && cur.blk == cur.nblk - 1 && wj == 0 && lane == 0) {
                         // the pair's last piece: describe the pair for the merge kernel
@@ -934,7 +1029,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     l_acc[h] = 0.f;
                 E_run = -100;
             }
-            cursor_next(cur, a, groups);
+            cursor_next<TILES>(cur, a, groups);
         }
         // ---- teardown (workers): tid 0 reports a timeout and lets the last raw Q copy land
         tc_fence_before();
@@ -951,7 +1046,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
         // ring stage j % RING takes block j once O^T of block j - RING has read its V;
         // lane 4t + c fetches the block id of box c of tile t a block ahead
         Cursor pre = c0;
-        int32_t idc = lane < 8 ? fetch_tile_box_id(a, pre, lane >> 2, lane & 3) : kNoBlock;
+        int32_t idc = lane < MD::BOXES ? fetch_tile_box_id<TILES>(a, pre, lane >> 2, lane & 3) : kNoBlock;
         int j = 0;
         for (; j < n; ++j) {
             const int r = j % RING;
@@ -959,10 +1054,15 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 !__all_sync(0xffffffffu, wait_phase(tfree + r, (uint32_t)(j / RING - 1) & 1u, abort_flag)))
                 break;
             Cursor nx = pre;
-            cursor_next(nx, a, groups);
-            const int32_t id_next = (lane < 8 && j + 1 < n) ? fetch_tile_box_id(a, nx, lane >> 2, lane & 3) : kNoBlock;
-            issue_block(a, pre, lane, idc, base + C::OFF_RING + r * C::STAGE, scl + r * 2 * BT, tfull + 2 * r,
-                        box_ok + r * C::BOXES);
+            cursor_next<TILES>(nx, a, groups);
+            const int32_t id_next =
+                (lane < MD::BOXES && j + 1 < n) ? fetch_tile_box_id<TILES>(a, nx, lane >> 2, lane & 3) : kNoBlock;
+            if (PAIR)
+                issue_block_pairs(a, pre, lane, idc, base + C::OFF_RING + r * C::STAGE, scl + r * 2 * C::SCL_TOK,
+                                  C::SCL_TOK, tfull + 2 * r, box_ok + r * C::BOXES);
+            else
+                issue_block<C::SCL_TOK>(a, pre, lane, idc, base + C::OFF_RING + r * C::STAGE,
+                                        scl + r * 2 * C::SCL_TOK, tfull + 2 * r, box_ok + r * C::BOXES);
             idc = id_next;
             pre = nx;
         }
@@ -1003,7 +1103,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     if (!wait_phase(kready + w, pj, abort_flag))
                         break;
                     tc_fence_after();
-                    const uint64_t qd = desc_add(qdesc0, (uint32_t)(piece & 1) * NH * D * 2);
+                    const uint64_t qd = desc_add(qdesc0, (uint32_t)(piece & 1) * C::QH_SLOT);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         umma_f16_ts(tmem + s_col, tmem + k_col + 8 * kk, desc_add(qd, kk * 2 * C::Q_SC), IDESC_QK,
@@ -1033,7 +1133,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     ++n_pv;
                     ++jw;
                 }
-                cursor_next(c, a, groups);
+                cursor_next<TILES>(c, a, groups);
             }
             if (*abort_flag) {
                 // let the tensor core finish what this thread issued: its last commit covers it all
@@ -1056,13 +1156,14 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
 }
 
 // Merge the pieces of one cut (sequence, head group) pair, 8 heads per CTA:
-// warp k takes head 8 blockIdx.y + k, lane d = 4 lane .. 4 lane + 3.  The
-// flash-decoding combine: M = max lse, w = exp(lse - M), out = sum w o / sum w.
+// warp k takes head 8 blockIdx.y + k of the group, lane d = 4 lane .. 4 lane + 3.
+// The flash-decoding combine: M = max lse, w = exp(lse - M), out = sum w o / sum w.
 // A cut pair's last piece always opens its CTA's share, so its descriptor is in
 // slot 0 of CTA blockIdx.x.
+template <bool PAIR>
 __global__ void __launch_bounds__(256) decode_tc_merge_kernel(const __grid_constant__ DecodeArgs a)
 {
-    constexpr int NH = TcCfg::NH, D = TcCfg::D;
+    constexpr int NHG = TcMode<PAIR>::NHG, D = TcMode<PAIR>::DH;
     griddep_wait();
     griddep_launch_dependents();
     const int *m = a.merge_desc + (2 * blockIdx.x) * 8;
@@ -1072,12 +1173,13 @@ __global__ void __launch_bounds__(256) decode_tc_merge_kernel(const __grid_const
     const int g = __ldg(m + 1), c_lo = __ldg(m + 2), c_hi = __ldg(m + 3), slot_lo = __ldg(m + 4);
     const int np = c_hi - c_lo + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int jh = blockIdx.y * 8 + warp, h = g * NH + jh;
-    if (h >= a.num_q_heads)
+    const int hs = min(a.num_q_heads, NHG);
+    const int jh = blockIdx.y * 8 + warp, h = g * NHG + jh;
+    if (jh >= hs || h >= a.num_q_heads)
         return;
     float M = -INFINITY;
     for (int p = lane; p < np; p += 32)
-        M = fmaxf(M, __ldg(a.lse + merge_row(c_lo, p, slot_lo, jh)));
+        M = fmaxf(M, __ldg(a.lse + merge_row(c_lo, p, slot_lo, jh, hs)));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -1089,10 +1191,11 @@ __global__ void __launch_bounds__(256) decode_tc_merge_kernel(const __grid_const
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int p = min(p0 + u, np - 1);
-            const size_t row = merge_row(c_lo, p, slot_lo, jh);
+            const size_t row = merge_row(c_lo, p, slot_lo, jh, hs);
             const float ls = __ldg(a.lse + row);
             wgt[u] = (p0 + u >= np || ls == -INFINITY || M == -INFINITY) ? 0.f : __expf(ls - M);
-            x[u] = __ldg(reinterpret_cast<const float4 *>(a.o_partial + row * D) + lane);
+            x[u] = 4 * lane < D ? __ldg(reinterpret_cast<const float4 *>(a.o_partial + row * D) + lane)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -1104,42 +1207,56 @@ __global__ void __launch_bounds__(256) decode_tc_merge_kernel(const __grid_const
         }
     }
     const float f = den > 0.f ? 1.f / den : 0.f;
+    if (4 * lane >= D)
+        return;
     uint2 o;
     o.x = pack_bf16x2(acc.x * f, acc.y * f);
     o.y = pack_bf16x2(acc.z * f, acc.w * f);
     *reinterpret_cast<uint2 *>(a.out + ((size_t)b * a.num_q_heads + h) * D + 4 * lane) = o;
 }
 
-cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s)
+namespace {
+
+template <bool PAIR>
+cudaError_t launch_decode_tc_t(const DecodeArgs &a, cudaStream_t s)
 {
     static std::atomic<int> attr_set{0};
     if (!attr_set.load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              TcCfg::SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
         // the kernel moves registers between its warpgroups (setmaxnreg): the split must fit
         // the registers it is launched with, or a group would wait for registers forever
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, decode_tc_kernel);
+        e = cudaFuncGetAttributes(&fa, decode_tc_kernel<PAIR>);
         if (e != cudaSuccess)
             return e;
         if (fa.numRegs != TcCfg::REG_LAUNCH)
             return cudaErrorInvalidConfiguration;
         attr_set.store(1, std::memory_order_release);
     }
-    cudaError_t e = launch_pdl(decode_tc_kernel, dim3(a.persist_ctas), dim3(TcCfg::THREADS), TcCfg::SMEM_BYTES, s, a);
+    cudaError_t e =
+        launch_pdl(decode_tc_kernel<PAIR>, dim3(a.persist_ctas), dim3(TcCfg::THREADS), TcCfg::SMEM_BYTES, s, a);
     if (e != cudaSuccess || !a.persistent)
         return e;
-    return launch_pdl(decode_tc_merge_kernel, dim3(a.persist_ctas, TcCfg::NH / 8), dim3(256), 0, s, a);
+    const int hs = a.num_q_heads < TcMode<PAIR>::NHG ? a.num_q_heads : TcMode<PAIR>::NHG;
+    return launch_pdl(decode_tc_merge_kernel<PAIR>, dim3(a.persist_ctas, (hs + 7) / 8), dim3(256), 0, s, a);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeArgs &a, int head_dim, cudaStream_t s)
+{
+    return head_dim == 64 ? launch_decode_tc_t<true>(a, s) : launch_decode_tc_t<false>(a, s);
 }
 
 int decode_tc_ctas_per_sm()
 {
     int n = 0;
-    cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM_BYTES);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_kernel, TcCfg::THREADS, TcCfg::SMEM_BYTES) !=
-        cudaSuccess)
+    cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM_BYTES);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_kernel<false>, TcCfg::THREADS,
+                                                      TcCfg::SMEM_BYTES) != cudaSuccess)
         n = 1;
     return n < 1 ? 1 : n;
 }

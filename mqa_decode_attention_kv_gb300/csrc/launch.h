@@ -43,35 +43,35 @@ struct AppendArgs {
 cudaError_t launch_quant_append(const AppendArgs &a, cudaStream_t s);
 
 struct DecodeArgs {
-    CUtensorMap k_map, v_map;          // 2-D maps over [num_blocks*page_size, head_dim] int8, 16-row boxes
-    CUtensorMap k_map64, v_map64;      // the same with 64-row boxes (tcgen05 kernel, page_size 64 only)
+    // 2-D maps over the int8 codes: head_dim 128, [num_blocks*page_size][128] in 16-row
+    // boxes (k_map64, v_map64: 64-row boxes, page_size 64 only); head_dim 64, two tokens
+    // a row, [num_blocks*page_size/2][128] in 8-row boxes
+    CUtensorMap k_map, v_map;
+    CUtensorMap k_map64, v_map64;
     const float *k_scale, *v_scale;
     const int32_t *block_table, *seq_lens;
     const __nv_bfloat16 *q;
-    __nv_bfloat16 *out;                // direct output (num_splits == 1)
-    float *o_partial, *lse;            // split output (num_splits > 1)
-    int32_t *counters;                 // [batch][head groups] zeroed tickets: fused merge, or null
+    __nv_bfloat16 *out;                // bf16 output (whole pairs directly; cut pairs by the merge kernel)
+    float *o_partial, *lse;            // partials of pairs cut between CTAs (balanced mode)
     int32_t *dev_status;
     int32_t batch, max_blocks, num_blocks, page_size, max_seq_len;
     int32_t ring;                      // > 0: window-bounded cache, page p in table entry p % ring
     int32_t num_q_heads, window;
-    int32_t tiles_per_split, num_splits;
     float q_scale_log2;                // sm_scale * log2(e)
-    // tcgen05 kernel only: persistent != 0 = balanced shares of the (sequence,
-    // head group, block) list over persist_ctas CTAs (partials in o_partial /
-    // lse rows [2 * persist_ctas][32], tickets in counters); 0 = one CTA per
-    // (sequence, head group), persist_ctas = batch * head groups
+    // persistent != 0 = balanced shares of the (sequence, head group, block) list
+    // over persist_ctas CTAs (partials in o_partial / lse rows [2 * persist_ctas]
+    // [heads of a group]); 0 = one CTA per (sequence, head group), persist_ctas =
+    // batch * head groups.  A head group is 32 query heads (head_dim 128) or 16
+    // (head_dim 64).
     int32_t persistent, persist_ctas;
     int32_t *merge_desc;               // [2 * persist_ctas][8]: cut pairs to merge (written by every call)
 };
-cudaError_t launch_decode(const DecodeArgs &a, int head_dim, cudaStream_t s);
-// head_dim 128 with 32 or 64 query heads runs on the tcgen05 kernel; the rest on the warp-MMA kernel
-inline bool decode_uses_tc(int head_dim, int num_q_heads) { return head_dim == 128 && num_q_heads >= 32; }
-cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t s);
-constexpr int kTcMaxCtas = 1024;   // balanced tcgen05 decode: at most this many CTAs (merge slots: 2 each)
+// Decode attention on the tcgen05 kernel (head_dim 64 or 128), then, in balanced
+// mode, the kernel that merges the pairs cut between CTAs.
+cudaError_t launch_decode_tc(const DecodeArgs &a, int head_dim, cudaStream_t s);
+constexpr int kTcMaxCtas = 1024;   // balanced decode: at most this many CTAs (merge slots: 2 each)
 int decode_tc_ctas_per_sm();
-int decode_ctas_per_sm(int head_dim, int num_q_heads);
-constexpr int kMaxFusedSplits = 16;  // the decode kernel merges up to this many splits itself
+inline int decode_heads_per_group(int head_dim) { return head_dim == 64 ? 16 : 32; }
 
 cudaError_t launch_combine(const float *o_partial, const float *lse, int32_t batch, int32_t num_splits,
                            int32_t num_q_heads, int32_t head_dim, __nv_bfloat16 *out, cudaStream_t s);

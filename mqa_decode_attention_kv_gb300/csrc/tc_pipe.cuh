@@ -132,19 +132,20 @@ __device__ __forceinline__ int box_row(const Args &a, int32_t id, int T, int c)
     return ok ? id * a.page_size + (T * kTileTokens + c * kChunkTokens) % a.page_size : -1;
 }
 
-// Block id of box c (16 tokens) of tile t (64 tokens, 0 or 1) of the block at
-// position p (fields b, blk, t_first, lo, L); kNoBlock when the box lies outside [lo, L).
-template <class Args, class Pos>
+// Block id of box c (16 tokens) of tile t (64 tokens, 0 .. TILES-1) of the block at
+// position p (fields b, blk, t_first, lo, L) of TILES tiles; kNoBlock when the box
+// lies outside [lo, L).
+template <int TILES = 2, class Args, class Pos>
 __device__ __forceinline__ int32_t fetch_tile_box_id(const Args &a, const Pos &p, int t, int c)
 {
-    const int T = p.t_first + 2 * p.blk + t;
+    const int T = p.t_first + TILES * p.blk + t;
     return T <= (p.L - 1) / kTileTokens
                ? fetch_box_block(a.block_table + (size_t)p.b * a.max_blocks, a.page_size, T, c, p.lo, p.L, a.ring)
                : kNoBlock;
 }
 
 // Both tiles of the block at p into ring stage `stage`, their token scales into
-// `scl` ([2][128] fp32: K, V).  Lane 4t + c holds the id of box c of tile t.
+// `scl` ([2][SCL_STRIDE] fp32: K, V).  Lane 4t + c holds the id of box c of tile t.
 // A tile inside [lo, L) on one 64-token page goes as one 64-row copy per tensor
 // (and one 256-byte copy per scale row), any other tile as its 16-row boxes
 // that overlap [lo, L) (and 64-byte scale copies).  `part` 0 issues the K codes
@@ -153,11 +154,11 @@ __device__ __forceinline__ int32_t fetch_tile_box_id(const Args &a, const Pos &p
 // (or only) warp records in oks[4t + c] whether box c comes.  The copies are
 // spread over the lanes: one copy instruction takes a thread a few hundred
 // cycles to issue, and the lanes' and warps' issues overlap.
-template <class Args, class Pos>
+template <int SCL_STRIDE = kBlockTokens, class Args, class Pos>
 __device__ __forceinline__ void issue_block(const Args &a, const Pos &p, int lane, int32_t idc, uint8_t *stage,
                                             float *scl, uint64_t *bars, uint32_t *oks, int part = -1)
 {
-    constexpr int D = kBlockD, CODES = kBlockTokens * kBlockD, BT = kBlockTokens;
+    constexpr int D = kBlockD, CODES = kBlockTokens * kBlockD;
     const int tb = lane >> 2, c = lane & 3;  // lanes 0-7: tile tb, box c
     const int Tb = p.t_first + 2 * p.blk + (tb & 1);
     const int row = lane < 8 ? box_row(a, idc, Tb, c) : -1;
@@ -187,7 +188,7 @@ __device__ __forceinline__ void issue_block(const Args &a, const Pos &p, int lan
             if (k == 0)
                 tma_load_2d(stage + q * CODES + t * kTileTokens * D, q ? &a.v_map64 : &a.k_map64, 0, r0, bars + t);
             else
-                bulk_load(scl + q * BT + t * kTileTokens, (q ? a.v_scale : a.k_scale) + r0, kTileTokens * 4, bars + t);
+                bulk_load(scl + q * SCL_STRIDE + t * kTileTokens, (q ? a.v_scale : a.k_scale) + r0, kTileTokens * 4, bars + t);
         }
     }
     // other tiles: lane 4t + c issues box c's codes and scales of the part(s)
@@ -195,9 +196,42 @@ __device__ __forceinline__ void issue_block(const Args &a, const Pos &p, int lan
         const int box = lane;
         for (int q = p_lo; q <= p_hi; ++q) {
             tma_load_2d(stage + q * CODES + box * kChunkTokens * D, q ? &a.v_map : &a.k_map, 0, row, bars + tb);
-            bulk_load(scl + q * BT + box * kChunkTokens, (q ? a.v_scale : a.k_scale) + row, kChunkTokens * 4,
+            bulk_load(scl + q * SCL_STRIDE + box * kChunkTokens, (q ? a.v_scale : a.k_scale) + row, kChunkTokens * 4,
                       bars + tb);
         }
+    }
+}
+
+// head_dim 64 read as rows of two tokens: a block is 128 rows of 128 bytes (256
+// tokens, four 64-token tiles), each 16-token box one 8-row copy per tensor
+// through maps over [num_blocks * page_size / 2][128] (a box never crosses a
+// page: 16 tokens divide both page sizes).  Lane c < 16 holds the id of box c
+// (tile c / 4, box c % 4 of it) and issues its codes and scales; token scales go
+// to scl[c * 16 ..] (K) and scl[scl_stride + c * 16 ..] (V).  Barrier bars[h]
+// takes boxes 8h .. 8h+7 (rows 64h .. 64h+63); oks[c] records whether box c comes.
+template <class Args, class Pos>
+__device__ __forceinline__ void issue_block_pairs(const Args &a, const Pos &p, int lane, int32_t idc,
+                                                  uint8_t *stage, float *scl, int scl_stride, uint64_t *bars,
+                                                  uint32_t *oks)
+{
+    constexpr int CODES = kBlockTokens * kBlockD, BOX_BYTES = 8 * kBlockD;
+    const int T = p.t_first + 4 * p.blk + (lane >> 2);
+    const int row = lane < 16 ? box_row(a, idc, T, lane & 3) : -1;  // cache row (token) of the box's first token
+    const uint32_t okall = __ballot_sync(0xffffffffu, row >= 0);
+    if (lane < 16)
+        oks[lane] = row >= 0 ? 1u : 0u;
+    __syncwarp();  // the flags are written before the arrival
+    if (lane < 2) {
+        const uint32_t n = (uint32_t)__popc((okall >> (8 * lane)) & 0xffu);
+        mbar_arrive_expect_tx(bars + lane, n * 2u * kChunkTokens * (kBlockD / 2 + 4));
+    }
+    __syncwarp();
+    if (lane < 16 && row >= 0) {
+        uint64_t *bar = bars + (lane >> 3);
+        tma_load_2d(stage + lane * BOX_BYTES, &a.k_map, 0, row >> 1, bar);
+        tma_load_2d(stage + CODES + lane * BOX_BYTES, &a.v_map, 0, row >> 1, bar);
+        bulk_load(scl + lane * kChunkTokens, a.k_scale + row, kChunkTokens * 4, bar);
+        bulk_load(scl + scl_stride + lane * kChunkTokens, a.v_scale + row, kChunkTokens * 4, bar);
     }
 }
 

@@ -52,9 +52,8 @@ def test_workspace_size_formula(L):
     r256 = lambda x: (x + 255) // 256 * 256
     part = 8 * 10 * 32 * 128 * 4           # fp32 partial outputs
     lse = 8 * 10 * 32 * 4                  # fp32 log-sum-exps
-    tickets = 8 * 1 * 4                    # one int32 per (sequence, group of 32 heads)
-    descs = 2 * 1024 * 8 * 4               # or the tcgen05 kernel's merge descriptors, if larger
-    assert n == r256(r256(part) + lse) + max(tickets, descs)
+    descs = 2 * 1024 * 8 * 4               # merge descriptors of up to 1024 CTAs
+    assert n == r256(r256(part) + lse) + descs
 
 
 def cache(num_blocks=16, page=16, d=64, **kw):

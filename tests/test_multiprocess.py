@@ -29,18 +29,20 @@ def torchrun(args, timeout=600):
 
 def test_barrier_and_max_over_ranks(tmp_path):
     script = tmp_path / "ranks.py"
+    # each rank writes its own file (two ranks printing at once may interleave on stdout)
     script.write_text(
-        "import json\n"
+        "import json, sys\n"
         "import bench\n"
         "rank, world, local = bench.rank_info()\n"
         "dist = bench.dist_setup(world, local)\n"
         "bench.barrier(dist)\n"
         "m = bench.reduce_max(dist, 1.5 + 2.0 * rank)\n"
         "bench.barrier(dist)\n"
-        "print(json.dumps({'rank': rank, 'world': world, 'max': m}), flush=True)\n")
-    r = torchrun([str(script)])
+        "with open(sys.argv[1] + f'/rank{rank}.json', 'w') as f:\n"
+        "    json.dump({'rank': rank, 'world': world, 'max': m}, f)\n")
+    r = torchrun([str(script), str(tmp_path)])
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    lines = [json.loads((tmp_path / f"rank{k}.json").read_text()) for k in range(2)]
     assert sorted(d["rank"] for d in lines) == [0, 1]
     assert all(d["world"] == 2 and d["max"] == 3.5 for d in lines)
 
