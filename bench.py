@@ -501,6 +501,9 @@ class PrefillWorkload:
         self.q = torch.randn((self.T, H, D), generator=gen, device=device).to(torch.bfloat16)
         self.out = [torch.empty_like(self.q) for _ in w.windows]
         self.max_q = new
+        # one workspace for every layer (the largest: the global layer's tile images)
+        self.ws = torch.empty(max(16, max(mk.mqa_prefill_workspace_size(w.batch, self.batch.max_seq_len, W, new, D)
+                                          for W in w.windows)), dtype=torch.uint8, device=device)
         self.lib = mk.lib()
         self._c = self.cache.c()
         self._carr = (mk._Cache * 1)(self._c)
@@ -520,8 +523,8 @@ class PrefillWorkload:
         w = self.w
         rc = self.lib.mqa_prefill_attn(self._carr, 1, self._lmap, len(w.windows), l, w.windows[l],
                                        ctypes.byref(self._bt), self.cu_q.data_ptr(), self.T, self.max_q,
-                                       self.q.data_ptr(), self.out[l].data_ptr(), w.num_q_heads, self.scale, None,
-                                       stream)
+                                       self.q.data_ptr(), self.out[l].data_ptr(), w.num_q_heads, self.scale,
+                                       self.ws.data_ptr(), self.ws.numel(), None, stream)
         assert rc == 0, rc
 
     def step(self, stream: int):
@@ -856,10 +859,16 @@ def run_mixed(args):
             if splits > 1:
                 ws = torch.empty(mk.mqa_decode_workspace_size(len(dec), H, D, splits), dtype=torch.uint8,
                                  device=device)
-            one = lambda: mk.mqa_prefill_attn([cache], [0], 0, W, batch, cu_q, q, chunk, stream=stream)
+            ws_one = torch.empty(max(16, mk.mqa_prefill_workspace_size(batch.batch, batch.max_seq_len, W, chunk, D)),
+                                 dtype=torch.uint8, device=device)
+            ws_ch = torch.empty(max(16, mk.mqa_prefill_workspace_size(b_ch.batch, b_ch.max_seq_len, W, chunk, D)),
+                                dtype=torch.uint8, device=device)
+            one = lambda: mk.mqa_prefill_attn([cache], [0], 0, W, batch, cu_q, q, chunk, workspace=ws_one,
+                                              stream=stream)
             two = lambda: (mk.mqa_decode_attn([cache], [0], 0, W, b_dec, q_dec, num_splits=splits, workspace=ws,
                                               stream=stream),
-                           mk.mqa_prefill_attn([cache], [0], 0, W, b_ch, cu_ch, q_ch, chunk, stream=stream))
+                           mk.mqa_prefill_attn([cache], [0], 0, W, b_ch, cu_ch, q_ch, chunk, workspace=ws_ch,
+                                               stream=stream))
             for name, fn in (("one_launch", one), ("two_launches", two)):
                 for _ in range(max(args.warmup, 1)):
                     fn()

@@ -30,7 +30,8 @@ MQA_DEV_TIMEOUT = 8
 MQA_MAX_SPLITS = 1024
 
 EXPORTED = ("kv_quant_append", "mqa_decode_attn", "mqa_decode_auto_splits", "mqa_decode_workspace_size",
-            "split_kv_combine", "mqa_prefill_attn", "mqa_status_str", "mqa_decode_attn_noalloc",
+            "split_kv_combine", "mqa_prefill_attn", "mqa_prefill_workspace_size", "mqa_status_str",
+            "mqa_decode_attn_noalloc",
             "mqa_pc_create", "mqa_pc_destroy", "mqa_pc_match", "mqa_pc_insert", "mqa_pc_offload",
             "mqa_pc_upload", "mqa_pc_stats")
 
@@ -72,8 +73,11 @@ def declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.mqa_decode_workspace_size.restype = sz
     L.split_kv_combine.argtypes = [P, P, i32, i32, i32, i32, P, P]
     L.split_kv_combine.restype = ctypes.c_int
-    L.mqa_prefill_attn.argtypes = [P, i32, P, i32, i32, i32, P, P, i32, i32, P, P, i32, ctypes.c_float, P, P]
+    L.mqa_prefill_attn.argtypes = [P, i32, P, i32, i32, i32, P, P, i32, i32, P, P, i32, ctypes.c_float, P, sz,
+                                   P, P]
     L.mqa_prefill_attn.restype = ctypes.c_int
+    L.mqa_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.mqa_prefill_workspace_size.restype = sz
     L.mqa_decode_attn_noalloc.argtypes = [P, i32, P, i32, i32, i32, P, P, P, i32, ctypes.c_float, i32, P, P]
     L.mqa_decode_attn_noalloc.restype = ctypes.c_int
     L.mqa_status_str.argtypes = [ctypes.c_int]
@@ -264,23 +268,33 @@ def split_kv_combine(o_partial, lse, out=None, stream=None):
     return out
 
 
+def mqa_prefill_workspace_size(batch: int, max_seq_len: int, window: int, max_q_len: int, head_dim: int) -> int:
+    return int(lib().mqa_prefill_workspace_size(batch, max_seq_len, window, max_q_len, head_dim))
+
+
 def mqa_prefill_attn(caches: Sequence[KVCache], layer_to_kv: Sequence[int], layer: int, window: int,
                      batch: Batch, cu_q, q, max_q_len: int, out=None, sm_scale: float | None = None,
-                     dev_status=None, stream=None):
+                     workspace=None, dev_status=None, stream=None):
     """Causal prefill attention of the ``cu_q``-described new tokens (bf16 q
-    [total_q, num_q_heads, head_dim]).  Returns ``out``."""
+    [total_q, num_q_heads, head_dim]).  ``workspace`` (uint8, on the device)
+    is allocated for the call when not given.  Returns ``out``."""
     import torch
     T, H, D = q.shape
     if out is None:
         out = torch.empty_like(q)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
+    need = mqa_prefill_workspace_size(batch.batch, batch.max_seq_len, window, max_q_len, D)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     carr = _caches_array(caches)
     lmap = (ctypes.c_int32 * len(layer_to_kv))(*layer_to_kv)
     bt = batch.c()
     rc = lib().mqa_prefill_attn(carr, len(caches), lmap, len(layer_to_kv), int(layer), int(window),
                                 ctypes.byref(bt), _ptr(cu_q), int(T), int(max_q_len), _ptr(q), _ptr(out),
-                                int(H), float(sm_scale), _ptr(dev_status), _stream(stream))
+                                int(H), float(sm_scale), _ptr(workspace),
+                                0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                _ptr(dev_status), _stream(stream))
     _check("mqa_prefill_attn", rc)
     return out
 

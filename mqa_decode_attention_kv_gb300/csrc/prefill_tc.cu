@@ -2,6 +2,16 @@
 // (tcgen05), head_dim 128, over the int8 paged cache (prefix-shared blocks
 // allowed).
 //
+// Two kernels.  kv_tile_images_kernel converts, once per sequence, every
+// 64-key tile its queries can see into an fp16 image laid out exactly as the
+// tensor core reads it (K with its codes' exponent bias, V exact), plus a
+// record of the tile's K and V scales (a negative K scale marks a key that no
+// query of the sequence sees or whose block id is bad), its largest V scale
+// and whether all 64 keys are valid; one extra all-invalid tile closes each
+// sequence.  Every CTA of the attention kernel then bulk-copies the images of
+// its blocks: the 128 / (query tokens per CTA) CTAs of a sequence share one
+// conversion instead of each converting every block.
+//
 // A CTA owns M = 128 consecutive query rows of one sequence: 128 / H query
 // tokens times all H heads (MQA: every row reads the same K/V; the rows of
 // tokens t and heads h are contiguous in q and out).  It walks the 128-key
@@ -29,17 +39,12 @@
 //               barrier that ORs the need) and one power-of-two bound 2^E of
 //               the V scales.  At the end each half normalises its 64 columns
 //               of the row of O.
-//   warps 8-11  converters: thread k owns key row k of every block.  K codes
-//               to fp16 (with their exponent bias +1152) into a K buffer,
-//               V codes to fp16 in place in the ring stage, the block's K and
-//               V scales (negative K scale = key not fetched or outside the
-//               CTA's key range) and the warp's largest V scale.
-//   warp 12     lane 0 issues every tcgen05.mma and commit, S(j) one block
+//   warp 8      lane 0 issues every tcgen05.mma and commit, S(j) one block
 //               ahead of O += P'(j-1) V(j-1); the warp owns the tensor memory.
-//   warp 13     TMA: block ids a block ahead, the codes and scales of each
-//               block into a ring stage once the O update that read the
-//               stage's previous block has completed.
-//   warps 14-15 idle (their registers go to the softmax and converter warps).
+//   warp 9      bulk copies: the two tile images and records of each block
+//               into a ring stage once the O update that read the stage's
+//               previous block has completed.
+//   warps 10-11 idle (their registers go to the softmax warps).
 //
 // Every wait is bounded: a wait that runs out raises a CTA abort flag, every
 // role leaves at its next check (the softmax warps all together, at the
@@ -58,61 +63,81 @@
 namespace mqa {
 namespace {
 
+// A tile image: fp16 K [64 keys][128 d] in the core layout of the K-major B
+// operand of S (8-key row groups 2048 B apart, 8-d column groups 128 B apart),
+// then fp16 V as two 8 KB pieces of the MN-major B operand of O (see PfCfg).
+constexpr int kTileImg = 2 * kTileTokens * kBlockD * 2;  // 32768
+// A tile record: fp32 K scales [64], V scales [64], then the largest V scale of the
+// valid keys, an all-valid flag (int) and two pad words.
+constexpr int kTileRec = (2 * kTileTokens + 4) * 4;      // 528
+
 struct PfCfg {
     static constexpr int D = kBlockD;            // 128
     static constexpr int M = 128;                // query rows per CTA
     static constexpr int BK = kBlockTokens;      // keys per block
-    static constexpr int BOXES = BK / kChunkTokens;
-    static constexpr int RING = 4;
-    static constexpr int THREADS = 512;
-    static constexpr int CV_WARP0 = 8, MMA_WARP = 12, TMA_WARP = 13;
+    static constexpr int RING = 3;
+    static constexpr int THREADS = 384;
+    static constexpr int MMA_WARP = 8, TMA_WARP = 9;
     static constexpr int BAR_SM = 1;  // named barrier of the two softmax warpgroups
-    static constexpr int REG_LAUNCH = (65536 / THREADS) / 8 * 8;  // 128
+    static constexpr int REG_LAUNCH = (65536 / THREADS) / 8 * 8;  // 168
     static constexpr int REG_CTRL = 56;
-    static constexpr int REG_WORK = ((REG_LAUNCH * THREADS - 128 * REG_CTRL) / 384) / 8 * 8;
-    static constexpr int CODES = BK * D;
-    static constexpr int STAGE = 2 * CODES;
+    static constexpr int REG_WORK = ((REG_LAUNCH * THREADS - 128 * REG_CTRL) / 256) / 8 * 8;
+    static constexpr int CODES = BK * D;  // bytes of one V half (see the V layout below)
+    // a ring stage: fp16 K of the block (its two tile images' K parts), fp16 V (their V
+    // pieces), the two tile records
+    static constexpr int ST_K = 0, ST_V = BK * D * 2, ST_REC = 2 * BK * D * 2;
+    static constexpr int STAGE = (ST_REC + 2 * kTileRec + 1023) / 1024 * 1024;
     // shared memory
     static constexpr int OFF_RING = 0;
-    static constexpr int OFF_KH = OFF_RING + RING * STAGE;        // [2] fp16 K [128 keys][128 d], core layout
-    static constexpr int OFF_SCL = OFF_KH + 2 * BK * D * 2;       // [RING][2][128] fp32 K, V token scales (TMA)
-    static constexpr int OFF_OK = OFF_SCL + RING * 2 * BK * 4;    // [RING][8] box arrived
-    static constexpr int SB_KS = 0, SB_VS = 512, SB_VMAX = 1024, SB_ALL = 1040, SB_BYTES = 1056;
-    static constexpr int OFF_SB = OFF_OK + RING * BOXES * 4;      // [2] ks[128], vs[128], vmax[4], all-valid[4]
-    static constexpr int OFF_XM = OFF_SB + 2 * SB_BYTES;          // [2 parity][2 halves][128] row maxima / sums
+    static constexpr int OFF_XM = OFF_RING + RING * STAGE;        // [2 parity][2 halves][128] row maxima / sums
     static constexpr int OFF_MISC = OFF_XM + 2 * 2 * M * 4;       // tmem base, abort flag
     static constexpr int OFF_MBAR = OFF_MISC + 64;
-    static constexpr int NBAR = 3 * RING + 9;
+    static constexpr int NBAR = 3 * RING + 5;
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
     // tensor memory: Q (fp16 pairs) | O | S [2]; P'(j) (fp16 pairs) replaces S(j) in its own
     // buffer once read: keys 0-63 at columns 0-31 of the buffer, keys 64-127 at 64-95
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t Q_COL = 0, O_COL = 64, S_COL = 192;
-    // core-matrix strides: K rows = keys (K-major B of S), V rows = keys (MN-major B of O, the
-    // same in-place layout as the decode kernel: token group warp j at 4096 j, groups 0, 1 in
-    // the K half, 2, 3 in the V half)
+    // core-matrix strides: K rows = keys (K-major B of S); V rows = keys (MN-major B of O): key
+    // 32 w + 8 g + i (w < 4, g < 4, i < 8) in half g / 2 (CODES bytes apart) at 4096 w +
+    // 2048 (g % 2) + 16 i, so a 16-key MMA step kk reads half kk % 2 at 4096 (kk / 2); tile t
+    // of the block holds w = 2t, 2t + 1, i.e. 8 KB at 8192 t of each half
     static constexpr uint32_t K_SR = 16 * 128;  // next 8 keys
     static constexpr uint32_t K_SC = 128;       // next 8 d
     static constexpr uint32_t V_SR = 16 * 128;  // next 8 keys (inside a 16-key MMA step)
     static constexpr uint32_t V_SC = 128;       // next 8 d
 };
 static_assert(PfCfg::SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(PfCfg::OFF_KH % 1024 == 0 && PfCfg::STAGE % 1024 == 0, "1024-byte alignment");
-static_assert(PfCfg::OFF_SCL % 16 == 0 && PfCfg::OFF_OK % 16 == 0 && PfCfg::OFF_SB % 16 == 0 &&
-                  PfCfg::SB_BYTES % 16 == 0 && PfCfg::OFF_MISC % 16 == 0 && PfCfg::OFF_MBAR % 8 == 0,
+static_assert(PfCfg::STAGE % 1024 == 0 && PfCfg::ST_V % 1024 == 0, "1024-byte alignment");
+static_assert(PfCfg::ST_REC % 16 == 0 && kTileRec % 16 == 0 && kTileImg % 16 == 0 && PfCfg::OFF_XM % 16 == 0 &&
+                  PfCfg::OFF_MISC % 16 == 0 && PfCfg::OFF_MBAR % 8 == 0,
               "16-byte alignment");
 static_assert(PfCfg::S_COL + 2 * 128 <= PfCfg::TMEM_COLS, "tensor memory");
-static_assert(128 * (3 * PfCfg::REG_WORK + PfCfg::REG_CTRL) <= PfCfg::REG_LAUNCH * PfCfg::THREADS &&
+static_assert(128 * (2 * PfCfg::REG_WORK + PfCfg::REG_CTRL) <= PfCfg::REG_LAUNCH * PfCfg::THREADS &&
                   PfCfg::REG_WORK >= PfCfg::REG_LAUNCH,
               "register split within the launch allocation");
 
 constexpr float kBiasK = 1152.f;  // K codes enter the tensor core as code + 1152 (exact in fp16)
 
-// The key range of a CTA as the TMA helpers see it: blocks of two 64-token
-// tiles from tile t_first, keys [lo, L).
-struct PfPos {
-    int b, blk, t_first, lo, L;
-};
+// A sequence's shape as both kernels read it: length L, query rows [q0, q0 + qlen),
+// the window start klo of its first query, its first tile tf and the nt tiles from
+// there to the one holding L - 1 (records 0 .. nt - 1, record nt all-invalid).
+// False for a sequence without query rows or with lengths the launch does not
+// allow (the attention kernel's CTA 0 reports those).
+__device__ __forceinline__ bool pf_seq_shape(const PrefillArgs &a, int b, int &L, int &q0, int &qlen, int &klo,
+                                             int &tf, int &nt)
+{
+    L = __ldg(a.seq_lens + b);
+    q0 = __ldg(a.cu_q + b);
+    const int q1 = __ldg(a.cu_q + b + 1);
+    qlen = q1 - q0;
+    if (L < 1 || L > a.max_seq_len || qlen < 1 || qlen > L || qlen > a.max_q_len || q0 < 0 || q1 > a.total_q)
+        return false;
+    klo = a.window > 0 ? max(0, L - qlen - a.window + 1) : 0;
+    tf = klo / kTileTokens;
+    nt = (L - 1) / kTileTokens - tf + 1;
+    return nt + 1 <= a.tiles_max;
+}
 
 __device__ __forceinline__ void pf_regs_inc()
 {
@@ -131,19 +156,15 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
     constexpr int D = C::D, RING = C::RING, BK = C::BK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint32_t *box_ok = reinterpret_cast<uint32_t *>(base + C::OFF_OK);
-    float *scl = reinterpret_cast<float *>(base + C::OFF_SCL);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + C::OFF_MISC + 4);
-    uint64_t *tfull = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][2] tiles landed (TMA)
+    uint64_t *tfull = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][2] tile images landed (copies)
     uint64_t *tfree = tfull + 2 * RING;  // [RING] stage free: O update of its block done (tensor core)
-    uint64_t *kvready = tfree + RING;    // [2] K fp16, V fp16 and the block's scales ready (4 converter warps)
-    uint64_t *sfull = kvready + 2;       // [2] S(j) done                                   (tensor core)
-    uint64_t *sbfree = sfull + 2;        // [2] the block's scales read                    (8 softmax warps)
-    uint64_t *pready = sbfree + 2;       // P'(j) written, S(j) read                       (8 softmax warps)
+    uint64_t *sfull = tfree + RING;      // [2] S(j) done                                   (tensor core)
+    uint64_t *pready = sfull + 2;        // P'(j) written, S(j) read                       (8 softmax warps)
     uint64_t *odone = pready + 1;        // O += P'(j) V(j) done                           (tensor core)
     uint64_t *qready = odone + 1;        // Q in tensor memory                             (4 softmax warps)
-    static_assert(3 * C::RING + 9 == C::NBAR, "barrier count");
+    static_assert(3 * C::RING + 5 == C::NBAR, "barrier count");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.num_q_heads;
@@ -155,11 +176,8 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             mbar_init(tfull + s, 1);
         for (int s = 0; s < RING; ++s)
             mbar_init(tfree + s, 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(kvready + s, 4);
+        for (int s = 0; s < 2; ++s)
             mbar_init(sfull + s, 1);
-            mbar_init(sbfree + s, 8);
-        }
         mbar_init(pready, 8);
         mbar_init(odone, 1);
         mbar_init(qready, 4);
@@ -224,17 +242,15 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             const int qa = __ldg(a.cu_q + bb), qb = __ldg(a.cu_q + bb + 1);
             if (Lb < 1 || Lb > a.max_seq_len)
                 set_status(a.dev_status, MQA_DEV_BAD_SEQLEN);
-            else if (qb - qa > Lb || qa < 0 || qb < qa || qb > a.total_q)
+            else if (qb - qa > Lb || qa < 0 || qb < qa || qb > a.total_q || qb - qa > a.max_q_len)
                 set_status(a.dev_status, MQA_DEV_BAD_CU);
         }
     }
 
     // ---- this CTA's rows and keys (every thread computes the same)
-    const int L = __ldg(a.seq_lens + b);
-    const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
-    const int qlen = q1 - q0;
-    const bool bad = L < 1 || L > a.max_seq_len || qlen > L || q0 < 0 || qlen < 0 || q1 > a.total_q;
-    const int ntok = (bad || past_end) ? 0 : min(qlen, t_begin + tpc) - t_begin;  // query tokens of this CTA
+    int L, q0, qlen, klo_seq, tf, nt;
+    const bool good = pf_seq_shape(a, b, L, q0, qlen, klo_seq, tf, nt);
+    const int ntok = (!good || past_end) ? 0 : min(qlen, t_begin + tpc) - t_begin;  // query tokens of this CTA
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -251,14 +267,15 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
     const int lo_max = W > 0 ? max(0, i_last - W + 1) : 0; // the window start of the latest row
     const int t_first = klo / kTileTokens;
     const int nb = (i_last / kTileTokens - t_first + 2) >> 1;  // 128-key blocks
-    PfPos pos0{b, 0, t_first, klo, i_last + 1};
+    // block j holds tiles t_first + 2j, +1: the sequence's records t_first + 2j - tf, +1 (the
+    // second of the last block may be the all-invalid record nt)
 
-    if (warp < C::CV_WARP0 + 4)
+    if (warp < C::MMA_WARP)
         pf_regs_inc();
     else
         pf_regs_dec();
 
-    if (warp < C::CV_WARP0) {
+    if (warp < C::MMA_WARP) {
         // ================================================================ softmax
         // two warpgroups: half hf takes keys 64 hf .. 64 hf + 63 of every block for all 128
         // rows; thread r of each half owns query row r (tensor-memory lane r).  Both halves keep
@@ -333,17 +350,19 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
         bool ok = true;
         int j = 0;
         for (; j < nb; ++j) {
-            const int b2 = j & 1;
-            ok &= wait_phase(kvready + b2, (uint32_t)(j >> 1) & 1u, abort_flag);
+            const int b2 = j & 1, rs = j % RING;
+            ok &= wait_phase(tfull + 2 * rs, (uint32_t)(j / RING) & 1u, abort_flag);
+            ok &= wait_phase(tfull + 2 * rs + 1, (uint32_t)(j / RING) & 1u, abort_flag);
             ok &= wait_phase(sfull + b2, (uint32_t)(j >> 1) & 1u, abort_flag);
             tc_fence_after();
-            const uint8_t *sb = base + C::OFF_SB + b2 * C::SB_BYTES;
-            const float *ks = reinterpret_cast<const float *>(sb + C::SB_KS) + 64 * hf;
-            const float *vs = reinterpret_cast<const float *>(sb + C::SB_VS) + 64 * hf;
+            // this half's keys are the block's tile hf: its record
+            const uint8_t *recs = base + C::OFF_RING + rs * C::STAGE + C::ST_REC;
+            const float *ks = reinterpret_cast<const float *>(recs + hf * kTileRec);
+            const float *vs = ks + kTileTokens;
             const int kb = (t_first + 2 * j) * kTileTokens + 64 * hf;  // first key of this half-block
-            // every row sees every key of the half-block, and every key was fetched
-            const int *allv = reinterpret_cast<const int *>(sb + C::SB_ALL);
-            const bool full = kb >= lo_max && kb + 63 <= i0 && allv[2 * hf] != 0 && allv[2 * hf + 1] != 0 && rvalid;
+            // every row sees every key of the half-block, and every key is valid
+            const bool full = kb >= lo_max && kb + 63 <= i0 && reinterpret_cast<const int *>(ks)[2 * kTileTokens + 1] != 0 &&
+                              rvalid;
             // ---- exponent arguments y = x + c (x the masked log2-domain score, -inf when masked),
             // as fp32 pairs: y = ((S g - b g) k_s) + c
             uint64_t y2[32];
@@ -385,10 +404,8 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
                 }
             }
             const float ymax = fmaxf(ymx[0], ymx[1]);
-            const float vmx = fmaxf(fmaxf(reinterpret_cast<const float *>(sb + C::SB_VMAX)[0],
-                                          reinterpret_cast<const float *>(sb + C::SB_VMAX)[1]),
-                                    fmaxf(reinterpret_cast<const float *>(sb + C::SB_VMAX)[2],
-                                          reinterpret_cast<const float *>(sb + C::SB_VMAX)[3]));
+            const float vmx = fmaxf(reinterpret_cast<const float *>(recs)[2 * kTileTokens],
+                                    reinterpret_cast<const float *>(recs + kTileRec)[2 * kTileTokens]);
             // the reference holds while every y <= 14 - E (p <= 2^8) and the V bound covers the block;
             // a row without a reference yet moves at its first key
             const bool need = (m_run == -INFINITY && ymax != -INFINITY) || !(ymax <= 14.f - (float)E_run) ||
@@ -466,10 +483,8 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(sbfree + b2);
+            if (lane == 0)
                 mbar_arrive(pready);
-            }
         }
         // ---- epilogue: out = O / (sum of p * 2^(6-E)), half hf writing d = 64 hf .. 64 hf + 63
         if (j == nb) {
@@ -502,128 +517,39 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
         if (tid == 0 && *abort_flag)
             set_status(a.dev_status, MQA_DEV_TIMEOUT);
         return;
-    } else if (warp < C::CV_WARP0 + 4) {
-        // ================================================================ converters
-        const int wj = warp - C::CV_WARP0;
-        const int kr = 32 * wj + lane;  // key row of every block
-        uint8_t *kh0 = base + C::OFF_KH;
-        bool ok = true;
-        for (int j = 0; j < nb; ++j) {
-            const int r = j % RING, b2 = j & 1;
-            uint8_t *st = base + C::OFF_RING + r * C::STAGE;
-            ok &= wait_phase(tfull + 2 * r + (wj >> 1), (uint32_t)(j / RING) & 1u, abort_flag);
-            if (j >= 2) {
-                // K buffer b2 was read by S(j-2); the scales of slot b2 by the softmax of block j-2
-                ok &= wait_phase(sfull + b2, (uint32_t)((j - 2) >> 1) & 1u, abort_flag);
-                ok &= wait_phase(sbfree + b2, (uint32_t)((j - 2) >> 1) & 1u, abort_flag);
-            }
-            if (__any_sync(0xffffffffu, !ok))
-                break;
-            const uint8_t *crow = st + kr * D;
-            // ---- K: 128 codes -> fp16 (+1152) into K buffer b2, row kr
-            uint8_t *kh = kh0 + b2 * BK * D * 2;
-            // (a loop, not unrolled: the kernel's instruction footprint is a bottleneck of its own)
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                uint4 kc[4];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    kc[jj] = *reinterpret_cast<const uint4 *>(crow + ((uint32_t)((4 * half + jj) ^ (kr & 7)) << 4));
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    uint32_t h8[8];
-                    const uint4 kv = kc[jj];
-                    const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t tt = w4[u] ^ 0x80808080u;
-                        h8[2 * u] = __byte_perm(tt, 0x64646464u, 0x5140);
-                        h8[2 * u + 1] = __byte_perm(tt, 0x64646464u, 0x7362);
-                    }
-                    const int dch = 16 * (4 * half + jj);  // d of the chunk
-                    *reinterpret_cast<uint4 *>(kh + core_off(kr, dch, C::K_SR, C::K_SC)) =
-                        make_uint4(h8[0], h8[1], h8[2], h8[3]);
-                    *reinterpret_cast<uint4 *>(kh + core_off(kr, dch + 8, C::K_SR, C::K_SC)) =
-                        make_uint4(h8[4], h8[5], h8[6], h8[7]);
-                }
-            }
-            // ---- V: fp16 in place over this warp's 8 KB of codes (its own key rows)
-            uint4 vc[D / 16];
-#pragma unroll
-            for (int c = 0; c < D / 16; ++c)
-                vc[c] = *reinterpret_cast<const uint4 *>(crow + C::CODES + ((uint32_t)(c ^ (kr & 7)) << 4));
-            __syncwarp();
-            {
-                const int gq = lane >> 3;
-                uint8_t *vb = st + (gq >> 1) * C::CODES + wj * 4096 + (gq & 1) * 2048 + (lane & 7) * 16;
-#pragma unroll
-                for (int c = 0; c < D / 16; ++c) {
-                    uint32_t v8[8];
-                    i8x4_to_f16x2x2(vc[c].x, v8[0], v8[1]);
-                    i8x4_to_f16x2x2(vc[c].y, v8[2], v8[3]);
-                    i8x4_to_f16x2x2(vc[c].z, v8[4], v8[5]);
-                    i8x4_to_f16x2x2(vc[c].w, v8[6], v8[7]);
-                    *reinterpret_cast<uint4 *>(vb + (2 * c) * C::V_SC) = make_uint4(v8[0], v8[1], v8[2], v8[3]);
-                    *reinterpret_cast<uint4 *>(vb + (2 * c + 1) * C::V_SC) = make_uint4(v8[4], v8[5], v8[6], v8[7]);
-                }
-            }
-            // ---- the block's scales: a negative K scale marks a key not fetched or outside the range
-            {
-                const int key = (t_first + 2 * j) * kTileTokens + kr;
-                const bool fetched = box_ok[r * C::BOXES + (kr >> 4)] != 0;
-                const bool valid = fetched && key >= klo && key <= i_last;
-                uint8_t *sb = base + C::OFF_SB + b2 * C::SB_BYTES;
-                const float ksv = scl[r * 2 * BK + kr], vsv = scl[r * 2 * BK + BK + kr];
-                reinterpret_cast<float *>(sb + C::SB_KS)[kr] = valid ? ksv : -1.f;
-                reinterpret_cast<float *>(sb + C::SB_VS)[kr] = valid ? vsv : 0.f;
-                float vm = valid ? vsv : 0.f;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
-                const bool allv = __all_sync(0xffffffffu, valid);
-                if (lane == 0) {
-                    reinterpret_cast<float *>(sb + C::SB_VMAX)[wj] = vm;
-                    reinterpret_cast<int *>(sb + C::SB_ALL)[wj] = allv ? 1 : 0;
-                }
-            }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(kvready + b2);
-        }
-        tc_fence_before();
-        bar_all();
-        return;
     } else if (warp == C::TMA_WARP) {
-        // ================================================================ TMA producer
-        if (lane == 0) {
-            const bool p64 = a.page_size == kTileTokens;
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.k_map64 : &a.k_map))
-                         : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(p64 ? &a.v_map64 : &a.v_map))
-                         : "memory");
-        }
-        PfPos pre = pos0;
-        int32_t idc = lane < 8 ? fetch_tile_box_id(a, pre, lane >> 2, lane & 3) : kNoBlock;
+        // ================================================================ image copies
+        // block j into ring stage j % RING once the O update of block j - RING has read it:
+        // lane 4t + k copies tile t's K image (k = 0), V pieces (k = 1, 2) or record (k = 3)
+        const int t = (lane >> 2) & 1, k = lane & 3;
         int j = 0;
         for (; j < nb; ++j) {
             const int r = j % RING;
             if (j >= RING &&
                 !__all_sync(0xffffffffu, wait_phase(tfree + r, (uint32_t)(j / RING - 1) & 1u, abort_flag)))
                 break;
-            PfPos nx = pre;
-            ++nx.blk;
-            const int32_t id_next = (lane < 8 && j + 1 < nb) ? fetch_tile_box_id(a, nx, lane >> 2, lane & 3) : kNoBlock;
-            issue_block(a, pre, lane, idc, base + C::OFF_RING + r * C::STAGE, scl + r * 2 * BK, tfull + 2 * r,
-                        box_ok + r * C::BOXES);
-            idc = id_next;
-            pre = nx;
+            uint8_t *st = base + C::OFF_RING + r * C::STAGE;
+            const size_t rec = (size_t)b * a.tiles_max + (t_first + 2 * j + t - tf);  // < tiles_max (pf_seq_shape)
+            if (lane < 2)
+                mbar_arrive_expect_tx(tfull + 2 * r + lane, kTileImg + kTileRec);
+            __syncwarp();
+            if (lane < 8) {
+                uint64_t *bar = tfull + 2 * r + t;
+                const uint8_t *img = a.img + rec * kTileImg;
+                if (k == 0)
+                    bulk_load(st + C::ST_K + t * (kTileImg / 2), img, kTileImg / 2, bar);
+                else if (k < 3)
+                    bulk_load(st + C::ST_V + (k - 1) * C::CODES + t * (kTileImg / 4), img + (kTileImg / 4) * (k + 1),
+                              kTileImg / 4, bar);
+                else
+                    bulk_load(st + C::ST_REC + t * kTileRec, a.srec + rec * kTileRec, kTileRec, bar);
+            }
         }
         if (*abort_flag && lane == 0) {
             // the copies still in flight land before the CTA leaves
             for (int jj = max(0, j - RING); jj < j; ++jj)
-                for (int t = 0; t < 2; ++t)
-                    mbar_wait_drain(tfull + 2 * (jj % RING) + t, (uint32_t)(jj / RING) & 1u);
+                for (int tt = 0; tt < 2; ++tt)
+                    mbar_wait_drain(tfull + 2 * (jj % RING) + tt, (uint32_t)(jj / RING) & 1u);
         }
         tc_fence_before();
         bar_all();
@@ -633,12 +559,12 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
         if (warp == C::MMA_WARP && lane == 0) {
             constexpr uint32_t IDESC_S = umma_idesc_f16(128, BK, false, false);
             constexpr uint32_t IDESC_O = umma_idesc_f16(128, D, false, true);
-            const uint64_t kdesc0 = umma_sdesc(smem_u32(base + C::OFF_KH), C::K_SC, C::K_SR);
-            const uint64_t vdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING), C::V_SR, C::V_SC);
+            const uint64_t kdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING + C::ST_K), C::K_SC, C::K_SR);
+            const uint64_t vdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING + C::ST_V), C::V_SR, C::V_SC);
             int n_s = 0, n_o = 0;
             // O += P'(k) V(k): P' from S buffer k & 1 (keys 16kk .. 16kk+15 at column
-            // 64 (kk / 4) + 8 (kk % 4)), V (fp16 in place in ring stage k % RING) from shared memory;
-            // 16-key step kk = key groups 2kk, 2kk+1 of converter warp kk / 2
+            // 64 (kk / 4) + 8 (kk % 4)), V (fp16 in ring stage k % RING) from shared memory;
+            // 16-key step kk = key groups 2kk, 2kk+1: half kk % 2 at 4096 (kk / 2)
             auto issue_o = [&](int k) -> bool {
                 if (!wait_phase(pready, (uint32_t)k & 1u, abort_flag))
                     return false;
@@ -659,10 +585,11 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
                 const int b2 = j & 1;
                 // S(j) = Q K(j)^T into S buffer b2: its last contents, P'(j-2), were read by the O
                 // update issued in the previous step (the tensor core runs this thread's MMAs in order)
-                if (!wait_phase(kvready + b2, (uint32_t)(j >> 1) & 1u, abort_flag))
+                if (!wait_phase(tfull + 2 * (j % RING), (uint32_t)(j / RING) & 1u, abort_flag) ||
+                    !wait_phase(tfull + 2 * (j % RING) + 1, (uint32_t)(j / RING) & 1u, abort_flag))
                     break;
                 tc_fence_after();
-                const uint64_t kd = desc_add(kdesc0, (uint32_t)b2 * BK * D * 2);
+                const uint64_t kd = desc_add(kdesc0, (uint32_t)(j % RING) * C::STAGE);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     umma_f16_ts(tmem + C::S_COL + (uint32_t)b2 * BK, tmem + C::Q_COL + 8 * kk,
@@ -691,6 +618,88 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
     }
 }
 
+// Tile record blockIdx.x of sequence blockIdx.y: 256 threads, 64 keys.  Keys
+// from the window start of the sequence's first query to L - 1 are valid
+// (their block ids inside the pool); any other key gets code 0, K scale -1
+// and V scale 0, and record nt (past the sequence's last tile) is all such
+// keys.  Codes are converted exactly: K to code + 1152 (the exponent-bias
+// form of its byte; the attention kernel takes the bias off), V to the code.
+__global__ void __launch_bounds__(256) kv_tile_images_kernel(const __grid_constant__ PrefillArgs a)
+{
+    griddep_wait();  // the appended keys are visible from here
+    griddep_launch_dependents();
+    const int b = blockIdx.y, idx = blockIdx.x, tid = threadIdx.x;
+    int L, q0, qlen, klo, tf, nt;
+    if (!pf_seq_shape(a, b, L, q0, qlen, klo, tf, nt) || idx > nt)
+        return;
+    const int T = tf + idx;
+    uint8_t *img = a.img + ((size_t)b * a.tiles_max + idx) * kTileImg;
+    float *rec = reinterpret_cast<float *>(a.srec + ((size_t)b * a.tiles_max + idx) * kTileRec);
+    __shared__ int s_row[kTileTokens];  // cache row of each key, -1 = not valid
+    __shared__ float s_vmax[2];
+    __shared__ int s_all[2];
+    if (tid < kTileTokens) {
+        const int pos = T * kTileTokens + tid;
+        int row = -1;
+        if (idx < nt && pos >= klo && pos < L) {
+            const int id = __ldg(a.block_table + (size_t)b * a.max_blocks + table_entry(pos / a.page_size, a.ring));
+            if (id >= 0 && id < a.num_blocks)
+                row = id * a.page_size + pos % a.page_size;
+            else
+                set_status(a.dev_status, MQA_DEV_BAD_BLOCK);
+        }
+        s_row[tid] = row;
+        const float vs = row >= 0 ? __ldg(a.v_scale + row) : 0.f;
+        rec[tid] = row >= 0 ? __ldg(a.k_scale + row) : -1.f;
+        rec[kTileTokens + tid] = vs;
+        float vm = vs;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+        const bool all = __all_sync(0xffffffffu, row >= 0);
+        if ((tid & 31) == 0) {
+            s_vmax[tid >> 5] = vm;
+            s_all[tid >> 5] = all ? 1 : 0;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        rec[2 * kTileTokens] = fmaxf(s_vmax[0], s_vmax[1]);
+        reinterpret_cast<int *>(rec)[2 * kTileTokens + 1] = s_all[0] & s_all[1];
+        rec[2 * kTileTokens + 2] = 0.f;
+        rec[2 * kTileTokens + 3] = 0.f;
+    }
+    // K part: 16-byte piece at byte o holds key 8 (o / 2048) + (o / 16) % 8, d = 8 ((o / 128) % 16) ..
+    for (int c = tid; c < kTileImg / 32; c += 256) {
+        const uint32_t o = 16u * c;
+        const int key = (int)(o >> 11) * 8 + (int)((o >> 4) & 7);
+        const int d0 = (int)((o >> 7) & 15) * 8;
+        const int row = s_row[key];
+        const uint2 w = row >= 0 ? __ldg(reinterpret_cast<const uint2 *>(a.k_codes + (size_t)row * kBlockD + d0))
+                                 : make_uint2(0u, 0u);
+        const uint32_t t0 = w.x ^ 0x80808080u, t1 = w.y ^ 0x80808080u;
+        *reinterpret_cast<uint4 *>(img + o) =
+            make_uint4(__byte_perm(t0, 0x64646464u, 0x5140), __byte_perm(t0, 0x64646464u, 0x7362),
+                       __byte_perm(t1, 0x64646464u, 0x5140), __byte_perm(t1, 0x64646464u, 0x7362));
+    }
+    // V part: piece h (8 KB) holds the keys 32 w + 8 g + i with g / 2 == h, the 16-byte piece at
+    // byte o of it key 32 (o / 4096) + 8 (2 h + (o / 2048) % 2) + (o / 16) % 8, d = 8 ((o / 128) % 16) ..
+    for (int c = tid; c < kTileImg / 32; c += 256) {
+        const uint32_t o = 16u * c;
+        const int h = (int)(o >> 13);
+        const uint32_t p = o & 8191u;
+        const int key = (int)(p >> 12) * 32 + (2 * h + (int)((p >> 11) & 1)) * 8 + (int)((p >> 4) & 7);
+        const int d0 = (int)((p >> 7) & 15) * 8;
+        const int row = s_row[key];
+        const uint2 w = row >= 0 ? __ldg(reinterpret_cast<const uint2 *>(a.v_codes + (size_t)row * kBlockD + d0))
+                                 : make_uint2(0u, 0u);
+        uint32_t v[4];
+        i8x4_to_f16x2x2(w.x, v[0], v[1]);
+        i8x4_to_f16x2x2(w.y, v[2], v[3]);
+        *reinterpret_cast<uint4 *>(img + kTileImg / 2 + o) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s)
 {
     static std::atomic<int> attr_set{0};
@@ -715,8 +724,26 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s)
     const long long tiles = ((long long)a.total_q + tpc - 1) / tpc + a.batch;
     if (tiles > 0x7fffffffll)
         return cudaErrorInvalidConfiguration;
-    dim3 grid((unsigned)tiles, 1, 1);
-    return launch_pdl(prefill_tc_kernel, grid, dim3(PfCfg::THREADS), PfCfg::SMEM_BYTES, s, a);
+    cudaError_t e = launch_pdl(kv_tile_images_kernel, dim3((unsigned)a.tiles_max, (unsigned)a.batch, 1), dim3(256),
+                               0, s, a);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(prefill_tc_kernel, dim3((unsigned)tiles, 1, 1), dim3(PfCfg::THREADS), PfCfg::SMEM_BYTES, s, a);
 }
+
+// Tile records per sequence a prefill of this shape needs (its tiles plus the all-invalid one):
+// see pf_seq_shape.
+int prefill_tiles_max(int max_seq_len, int window, int max_q_len)
+{
+    long long t = ((long long)max_seq_len - 1) / kTileTokens + 1;
+    if (window > 0) {
+        const long long w = ((long long)window + max_q_len - 2) / kTileTokens + 2;
+        t = w < t ? w : t;
+    }
+    return (int)(t + 1);
+}
+
+size_t prefill_tile_image_bytes() { return kTileImg; }
+size_t prefill_tile_record_bytes() { return kTileRec; }
 
 }  // namespace mqa

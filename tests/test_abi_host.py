@@ -143,11 +143,31 @@ def test_combine_and_prefill_validation(L):
     arr = (mk._Cache * 1)(cache())
     lm = (ctypes.c_int32 * 1)(0)
     P = L.mqa_prefill_attn
-    assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), FAKE, 0, 0, FAKE, FAKE, 8, 0.1, None, None) == mk.MQA_OK
-    assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), None, 5, 3, FAKE, FAKE, 8, 0.1, None, None) == mk.MQA_ERR_INVALID_ARG
-    assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), FAKE, 5, 65, FAKE, FAKE, 8, 0.1, None, None) == mk.MQA_ERR_INVALID_ARG
-    assert P(arr, 1, lm, 1, 0, -3, ctypes.byref(b), FAKE, 5, 3, FAKE, FAKE, 8, 0.1, None, None) == mk.MQA_ERR_INVALID_ARG
-    assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), FAKE, 5, 3, FAKE, FAKE, 24, 0.1, None, None) == mk.MQA_ERR_UNSUPPORTED
+    assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), FAKE, 0, 0, FAKE, FAKE, 8, 0.1, None, 0, None, None) == mk.MQA_OK
+    assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), None, 5, 3, FAKE, FAKE, 8, 0.1, None, 0, None, None) == mk.MQA_ERR_INVALID_ARG
+    assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), FAKE, 5, 65, FAKE, FAKE, 8, 0.1, None, 0, None, None) == mk.MQA_ERR_INVALID_ARG
+    assert P(arr, 1, lm, 1, 0, -3, ctypes.byref(b), FAKE, 5, 3, FAKE, FAKE, 8, 0.1, None, 0, None, None) == mk.MQA_ERR_INVALID_ARG
+    assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), FAKE, 5, 3, FAKE, FAKE, 24, 0.1, None, 0, None, None) == mk.MQA_ERR_UNSUPPORTED
+    # head_dim 128 converts the key tiles into a workspace first: missing or short -> rejected
+    arr128 = (mk._Cache * 1)(cache(d=128, page=64))
+    b128, k128 = batch(max_blocks=4, max_seq_len=256, lens=[200, 130])
+    need = mk.mqa_prefill_workspace_size(2, 256, 0, 3, 128)
+    assert need > 0 and mk.mqa_prefill_workspace_size(2, 256, 0, 3, 64) == 0
+    assert P(arr128, 1, lm, 1, 0, 0, ctypes.byref(b128), FAKE, 5, 3, FAKE, FAKE, 32, 0.1, None, 0, None,
+             None) == mk.MQA_ERR_WORKSPACE
+    assert P(arr128, 1, lm, 1, 0, 0, ctypes.byref(b128), FAKE, 5, 3, FAKE, FAKE, 32, 0.1, FAKE, need - 1, None,
+             None) == mk.MQA_ERR_WORKSPACE
+
+
+def test_prefill_workspace_formula(L):
+    r256 = lambda x: (x + 255) // 256 * 256
+    # per sequence: the tiles of the key range plus one all-invalid tile; 32 KiB images, 528-byte records
+    for B, Lmax, W, Q in ((3, 8704, 0, 512), (256, 8704, 1024, 512), (5, 100, 1024, 7), (2, 64, 0, 64)):
+        tiles = -(-Lmax // 64)
+        if W > 0:
+            tiles = min(tiles, (W + Q - 2) // 64 + 2)
+        n = B * (tiles + 1)
+        assert mk.mqa_prefill_workspace_size(B, Lmax, W, Q, 128) == r256(n * 32768) + n * 528
 
 
 def test_auto_splits_validation(L):
@@ -179,7 +199,7 @@ def test_ring_argument_validation(L):
 
     def prefill(b, window, max_q):
         return L.mqa_prefill_attn(arr, 1, lm, 1, 0, window, ctypes.byref(b), FAKE, 10, max_q, FAKE, FAKE, 8,
-                                  0.125, None, None)
+                                  0.125, None, 0, None, None)
     br, kr = batch(lens=[100, 90], max_seq_len=100, ring_blocks=4)
     assert prefill(br, 16, 34) == mk.MQA_ERR_INVALID_ARG   # (16 + 34 - 2) / 16 + 2 = 5 pages > 4
     assert prefill(br, 49, 1) == mk.MQA_ERR_INVALID_ARG    # (49 + 1 - 2) / 16 + 2 = 5 pages > 4
