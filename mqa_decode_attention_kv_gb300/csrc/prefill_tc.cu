@@ -351,9 +351,10 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
         int j = 0;
         for (; j < nb; ++j) {
             const int b2 = j & 1, rs = j % RING;
-            ok &= wait_phase(tfull + 2 * rs, (uint32_t)(j / RING) & 1u, abort_flag);
-            ok &= wait_phase(tfull + 2 * rs + 1, (uint32_t)(j / RING) & 1u, abort_flag);
-            ok &= wait_phase(sfull + b2, (uint32_t)(j >> 1) & 1u, abort_flag);
+            // (the copies and S(j) have usually completed long before: tests first)
+            ok &= wait_done(tfull + 2 * rs, (uint32_t)(j / RING) & 1u, abort_flag);
+            ok &= wait_done(tfull + 2 * rs + 1, (uint32_t)(j / RING) & 1u, abort_flag);
+            ok &= wait_done(sfull + b2, (uint32_t)(j >> 1) & 1u, abort_flag);
             tc_fence_after();
             // this half's keys are the block's tile hf: its record
             const uint8_t *recs = base + C::OFF_RING + rs * C::STAGE + C::ST_REC;

@@ -18,6 +18,13 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volat
     return mbar_try_wait(bar, parity) || wait_phase_slow(bar, parity, abort_flag);
 }
 
+// For a wait that is usually satisfied already: a test of the phase first
+// (mbarrier.test_wait costs ~37 cycles against ~57 for try_wait on GB300).
+__device__ __forceinline__ bool wait_done(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    return mbar_test(bar, parity) || wait_phase(bar, parity, abort_flag);
+}
+
 // The polling loop (inlined: a called function could not serve warpgroups that
 // run with different register counts).
 __device__ __forceinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
