@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 const int r = i % RING;
                 const int pj = jw & 1;  // phase parity of this group's per-block barriers
                 uint8_t *st = base + C::OFF_RING + r * C::STAGE;
-                ok &= wait_phase(tfull + 2 * r + (wj >> 1), (uint32_t)(i / RING) & 1u, abort_flag);
+                ok &= wait_done(tfull + 2 * r + (wj >> 1), (uint32_t)(i / RING) & 1u, abort_flag);
                 tc_fence_after();
                 const uint8_t *crow = st + tok * D;  // this row's codes (K, then V at + CODES)
                 // the row's token(s): pos0 (and pos0 + 1 with pairs), in one box
@@ -740,13 +740,13 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                 // O^T of this group's previous block done: its P' buffer and O are free, and the MMA
                 // thread has consumed that block's vready / pready phases (no phase can be lapped)
                 if (jw >= 1)
-                    ok &= wait_phase(odone + w, (uint32_t)(pj ^ 1), abort_flag);
+                    ok &= wait_done(odone + w, (uint32_t)(pj ^ 1), abort_flag);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(vready + w);
                 // ---- scores of this row: S^T(i) row tok, 32 columns
-                ok &= wait_phase(sfull + w, (uint32_t)pj, abort_flag);
+                ok &= wait_done(sfull + w, (uint32_t)pj, abort_flag);
                 tc_fence_after();
                 uint32_t sr[NH];
                 tmem_ld32(tmem + lane_base + s_col, sr);
@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                     const uint32_t pj = (uint32_t)jw & 1u;
                     // S^T(i) = K(i) Q^T: K from the group's tensor memory, Q (the piece's slot) from
                     // shared memory; the group read its S buffer's previous contents before K(i)
-                    if (!wait_phase(kready + w, pj, abort_flag))
+                    if (!wait_done(kready + w, pj, abort_flag))
                         break;
                     tc_fence_after();
                     const uint64_t qd = desc_add(qdesc0, (uint32_t)(piece & 1) * C::QH_SLOT);
@@ -1110,7 +1110,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) decode_tc_kernel(const __gr
                                     kk > 0);
                     umma_commit(sfull + w);
                     ++n_s;
-                    if (!wait_phase(pready + w, pj, abort_flag) || !wait_phase(vready + w, pj, abort_flag))
+                    if (!wait_done(pready + w, pj, abort_flag) || !wait_done(vready + w, pj, abort_flag))
                         break;
                     // the group's first update of a piece overwrites O buffer piece & 1, last read by
                     // the epilogue of piece - 2
