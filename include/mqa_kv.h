@@ -196,10 +196,9 @@ int split_kv_combine(const float *o_partial, const float *lse, int32_t batch, in
  *              with more query tokens is skipped and flagged MQA_DEV_BAD_CU).
  *   q, out:    bf16 [total_q][num_q_heads][head_dim], 16-byte aligned.
  *   workspace: device scratch of mqa_prefill_workspace_size(...) bytes
- *              (16-byte aligned; may be NULL when that size is 0).  At head_dim
- *              128 the call first converts, once per sequence, every key tile
- *              its queries can see to fp16 there; its contents on entry do not
- *              matter.
+ *              (16-byte aligned).  The call first converts, once per sequence,
+ *              every key tile its queries can see to fp16 there; its contents on
+ *              entry do not matter.
  * Returns MQA_OK, or MQA_ERR_WORKSPACE if the workspace is missing or too small. */
 int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_t *layer_to_kv,
                      int32_t num_layers, int32_t layer, int32_t window, const mqa_batch *batch,
@@ -210,10 +209,10 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
 /* Bytes of prefill workspace for a batch of `batch` sequences of at most
  * max_seq_len keys and max_q_len query tokens, at this window and head_dim:
  * per sequence, T = min(ceil(max_seq_len / 64), (window + max_q_len - 2) / 64
- * + 2 when window > 0) + 1 tiles of 64 keys, each a 32 KiB fp16 image (K and V
- * as the tensor core reads them) and a 528-byte record (K and V scales, the
- * largest V scale, an all-valid flag), the records after the images (256-byte
- * aligned).  0 for head_dim 64. */
+ * + 2 when window > 0) + 1 tiles of 64 keys, each a 256 * head_dim byte fp16
+ * image (K and V as the tensor core reads them) and a 528-byte record (K and V
+ * scales, the largest V scale, an all-valid flag), the records after the
+ * images (256-byte aligned).  0 for an unsupported head_dim. */
 size_t mqa_prefill_workspace_size(int32_t batch, int32_t max_seq_len, int32_t window, int32_t max_q_len,
                                   int32_t head_dim);
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmqa_kv.so")
-SOURCES = ["api.cu", "quant_append.cu", "decode_tc.cu", "combine.cu", "prefill.cu", "prefill_tc.cu",
+SOURCES = ["api.cu", "quant_append.cu", "decode_tc.cu", "combine.cu", "prefill_tc.cu",
            "no_alloc.cu", "prefix_cache.cu"]
 HEADERS = ["common.cuh", "kv_stage.cuh", "launch.h", "tc.cuh", "tc_pipe.cuh"]
 

@@ -459,10 +459,10 @@ int split_kv_combine(const float *o_partial, const float *lse, int32_t batch, in
 size_t mqa_prefill_workspace_size(int32_t batch, int32_t max_seq_len, int32_t window, int32_t max_q_len,
                                   int32_t head_dim)
 {
-    if (head_dim != 128 || batch <= 0 || max_seq_len <= 0 || max_q_len <= 0 || window < 0)
+    if (!head_dim_ok(head_dim) || batch <= 0 || max_seq_len <= 0 || max_q_len <= 0 || window < 0)
         return 0;
     const size_t recs = (size_t)batch * prefill_tiles_max(max_seq_len, window, max_q_len);
-    return round256(recs * prefill_tile_image_bytes()) + recs * prefill_tile_record_bytes();
+    return round256(recs * prefill_tile_image_bytes(head_dim)) + recs * prefill_tile_record_bytes();
 }
 
 int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32_t *layer_to_kv,
@@ -493,13 +493,6 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
     const int D = cache->head_dim;
     PrefillArgs a;
     std::memset(&a, 0, sizeof a);
-    if (D == 64) {
-        // the warp-MMA kernel's tiles: 16-row TMA boxes
-        if ((rc = make_code_map(&a.k_map, cache->k_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
-            return rc;
-        if ((rc = make_code_map(&a.v_map, cache->v_codes, cache->num_blocks, cache->page_size, D)) != MQA_OK)
-            return rc;
-    }
     a.k_codes = cache->k_codes;
     a.v_codes = cache->v_codes;
     a.k_scale = cache->k_scale;
@@ -521,16 +514,14 @@ int mqa_prefill_attn(const mqa_kv_cache *caches, int32_t num_caches, const int32
     a.total_q = total_q;
     a.max_q_len = max_q_len;
     a.q_scale_log2 = sm_scale * 1.4426950408889634f;
-    if (D == 128) {
-        // the tile images and records: [batch][tiles_max] each
-        const size_t need = mqa_prefill_workspace_size(batch->batch, batch->max_seq_len, window, max_q_len, D);
-        if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
-            return MQA_ERR_WORKSPACE;
-        a.tiles_max = prefill_tiles_max(batch->max_seq_len, window, max_q_len);
-        a.img = static_cast<uint8_t *>(workspace);
-        a.srec = a.img + round256((size_t)batch->batch * a.tiles_max * prefill_tile_image_bytes());
-    }
-    return launch_prefill(a, D, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
+    // the tile images and records: [batch][tiles_max] each
+    const size_t need = mqa_prefill_workspace_size(batch->batch, batch->max_seq_len, window, max_q_len, D);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+        return MQA_ERR_WORKSPACE;
+    a.tiles_max = prefill_tiles_max(batch->max_seq_len, window, max_q_len);
+    a.img = static_cast<uint8_t *>(workspace);
+    a.srec = a.img + round256((size_t)batch->batch * a.tiles_max * prefill_tile_image_bytes(D));
+    return launch_prefill_tc(a, D, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MQA_OK : MQA_ERR_CUDA;
 }
 
 }  // extern "C"

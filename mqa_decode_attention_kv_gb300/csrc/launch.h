@@ -77,8 +77,7 @@ cudaError_t launch_combine(const float *o_partial, const float *lse, int32_t bat
                            int32_t num_q_heads, int32_t head_dim, __nv_bfloat16 *out, cudaStream_t s);
 
 struct PrefillArgs {
-    CUtensorMap k_map, v_map;          // head_dim 64: 16-row boxes
-    const int8_t *k_codes, *v_codes;   // head_dim 128: read by the tile-image pass
+    const int8_t *k_codes, *v_codes;   // read by the tile-image pass
     const float *k_scale, *v_scale;
     const int32_t *block_table, *seq_lens, *cu_q;
     const __nv_bfloat16 *q;
@@ -88,15 +87,14 @@ struct PrefillArgs {
     int32_t ring;                      // > 0: window-bounded cache, page p in table entry p % ring
     int32_t num_q_heads, window, total_q, max_q_len;
     float q_scale_log2;
-    // head_dim 128: the workspace's fp16 tile images [batch][tiles_max] and their scale records
+    // the workspace's fp16 tile images [batch][tiles_max] and their scale records
     uint8_t *img, *srec;
     int32_t tiles_max;
 };
-cudaError_t launch_prefill(const PrefillArgs &a, int head_dim, cudaStream_t s);
-// head_dim 128: the tile-image pass, then the tcgen05 attention kernel
-cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
+// The tile-image pass, then the tcgen05 attention kernel (head_dim 64 or 128).
+cudaError_t launch_prefill_tc(const PrefillArgs &a, int head_dim, cudaStream_t s);
 int prefill_tiles_max(int max_seq_len, int window, int max_q_len);
-size_t prefill_tile_image_bytes();
+size_t prefill_tile_image_bytes(int head_dim);
 size_t prefill_tile_record_bytes();
 
 }  // namespace mqa

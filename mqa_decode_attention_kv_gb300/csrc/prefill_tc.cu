@@ -1,6 +1,6 @@
 // Chunked causal prefill attention on the 5th-generation tensor cores
-// (tcgen05), head_dim 128, over the int8 paged cache (prefix-shared blocks
-// allowed).
+// (tcgen05), head_dim 64 or 128, over the int8 paged cache (prefix-shared
+// blocks allowed).
 //
 // Two kernels.  kv_tile_images_kernel converts, once per sequence, every
 // 64-key tile its queries can see into an fp16 image laid out exactly as the
@@ -63,19 +63,24 @@
 namespace mqa {
 namespace {
 
-// A tile image: fp16 K [64 keys][128 d] in the core layout of the K-major B
-// operand of S (8-key row groups 2048 B apart, 8-d column groups 128 B apart),
-// then fp16 V as two 8 KB pieces of the MN-major B operand of O (see PfCfg).
-constexpr int kTileImg = 2 * kTileTokens * kBlockD * 2;  // 32768
+// A tile image (head_dim D): fp16 K [64 keys][D] in the core layout of the
+// K-major B operand of S (8-key row groups D / 8 * 128 B apart, 8-d column groups
+// 128 B apart), then fp16 V as two pieces of 64 * D bytes of the MN-major B
+// operand of O (see PfCfg).
+template <int D>
+constexpr int tile_img_bytes() { return 2 * kTileTokens * D * 2; }
 // A tile record: fp32 K scales [64], V scales [64], then the largest V scale of the
 // valid keys, an all-valid flag (int) and two pad words.
 constexpr int kTileRec = (2 * kTileTokens + 4) * 4;      // 528
 
+template <int D_>
 struct PfCfg {
-    static constexpr int D = kBlockD;            // 128
+    static constexpr int D = D_;                 // head_dim: 64 or 128
+    static constexpr int IMG = tile_img_bytes<D>();
+    static constexpr int RS = D / 8 * 128;       // bytes between 8-row groups of the K and V layouts
     static constexpr int M = 128;                // query rows per CTA
     static constexpr int BK = kBlockTokens;      // keys per block
-    static constexpr int RING = 3;
+    static constexpr int RING = D == 64 ? 4 : 3;  // (head_dim 64: also keeps one CTA per SM)
     static constexpr int THREADS = 384;
     static constexpr int MMA_WARP = 8, TMA_WARP = 9;
     static constexpr int BAR_SM = 1;  // named barrier of the two softmax warpgroups
@@ -83,6 +88,7 @@ struct PfCfg {
     static constexpr int REG_CTRL = 56;
     static constexpr int REG_WORK = ((REG_LAUNCH * THREADS - 128 * REG_CTRL) / 256) / 8 * 8;
     static constexpr int CODES = BK * D;  // bytes of one V half (see the V layout below)
+    static constexpr int V_W = 2 * RS;    // bytes of a 32-key group inside a V half
     // a ring stage: fp16 K of the block (its two tile images' K parts), fp16 V (their V
     // pieces), the two tile records
     static constexpr int ST_K = 0, ST_V = BK * D * 2, ST_REC = 2 * BK * D * 2;
@@ -92,30 +98,29 @@ struct PfCfg {
     static constexpr int OFF_XM = OFF_RING + RING * STAGE;        // [2 parity][2 halves][128] row maxima / sums
     static constexpr int OFF_MISC = OFF_XM + 2 * 2 * M * 4;       // tmem base, abort flag
     static constexpr int OFF_MBAR = OFF_MISC + 64;
-    static constexpr int NBAR = 3 * RING + 5;
+    static constexpr int NBAR = 3 * RING + 6;
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
     // tensor memory: Q (fp16 pairs) | O | S [2]; P'(j) (fp16 pairs) replaces S(j) in its own
     // buffer once read: keys 0-63 at columns 0-31 of the buffer, keys 64-127 at 64-95
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t Q_COL = 0, O_COL = 64, S_COL = 192;
     // core-matrix strides: K rows = keys (K-major B of S); V rows = keys (MN-major B of O): key
-    // 32 w + 8 g + i (w < 4, g < 4, i < 8) in half g / 2 (CODES bytes apart) at 4096 w +
-    // 2048 (g % 2) + 16 i, so a 16-key MMA step kk reads half kk % 2 at 4096 (kk / 2); tile t
-    // of the block holds w = 2t, 2t + 1, i.e. 8 KB at 8192 t of each half
-    static constexpr uint32_t K_SR = 16 * 128;  // next 8 keys
-    static constexpr uint32_t K_SC = 128;       // next 8 d
-    static constexpr uint32_t V_SR = 16 * 128;  // next 8 keys (inside a 16-key MMA step)
-    static constexpr uint32_t V_SC = 128;       // next 8 d
+    // 32 w + 8 g + i (w < 4, g < 4, i < 8) in half g / 2 (CODES bytes apart) at V_W w + RS (g % 2)
+    // + 16 i, so a 16-key MMA step kk reads half kk % 2 at V_W (kk / 2); tile t of the block
+    // holds w = 2t, 2t + 1, i.e. 64 * D bytes at 64 * D * t of each half
+    static constexpr uint32_t K_SR = RS;   // next 8 keys
+    static constexpr uint32_t K_SC = 128;  // next 8 d
+    static constexpr uint32_t V_SR = RS;   // next 8 keys (inside a 16-key MMA step)
+    static constexpr uint32_t V_SC = 128;  // next 8 d
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(STAGE % 1024 == 0 && ST_V % 1024 == 0, "1024-byte alignment");
+    static_assert(ST_REC % 16 == 0 && kTileRec % 16 == 0 && IMG % 64 == 0 && OFF_XM % 16 == 0 && OFF_MISC % 16 == 0 &&
+                      OFF_MBAR % 8 == 0,
+                  "16-byte alignment");
+    static_assert(O_COL + D <= S_COL && S_COL + 2 * 128 <= TMEM_COLS && Q_COL + D / 2 <= O_COL, "tensor memory");
+    static_assert(128 * (2 * REG_WORK + REG_CTRL) <= REG_LAUNCH * THREADS && REG_WORK >= REG_LAUNCH,
+                  "register split within the launch allocation");
 };
-static_assert(PfCfg::SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(PfCfg::STAGE % 1024 == 0 && PfCfg::ST_V % 1024 == 0, "1024-byte alignment");
-static_assert(PfCfg::ST_REC % 16 == 0 && kTileRec % 16 == 0 && kTileImg % 16 == 0 && PfCfg::OFF_XM % 16 == 0 &&
-                  PfCfg::OFF_MISC % 16 == 0 && PfCfg::OFF_MBAR % 8 == 0,
-              "16-byte alignment");
-static_assert(PfCfg::S_COL + 2 * 128 <= PfCfg::TMEM_COLS, "tensor memory");
-static_assert(128 * (2 * PfCfg::REG_WORK + PfCfg::REG_CTRL) <= PfCfg::REG_LAUNCH * PfCfg::THREADS &&
-                  PfCfg::REG_WORK >= PfCfg::REG_LAUNCH,
-              "register split within the launch allocation");
 
 constexpr float kBiasK = 1152.f;  // K codes enter the tensor core as code + 1152 (exact in fp16)
 
@@ -141,18 +146,21 @@ __device__ __forceinline__ bool pf_seq_shape(const PrefillArgs &a, int b, int &L
 
 __device__ __forceinline__ void pf_regs_inc()
 {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PfCfg::REG_WORK));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PfCfg<128>::REG_WORK));
 }
 __device__ __forceinline__ void pf_regs_dec()
 {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfCfg::REG_CTRL));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfCfg<128>::REG_CTRL));
 }
+static_assert(PfCfg<64>::REG_WORK == PfCfg<128>::REG_WORK && PfCfg<64>::REG_CTRL == PfCfg<128>::REG_CTRL,
+              "one register split");
 
 }  // namespace
 
-__global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a)
+template <int D_>
+__global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a)
 {
-    using C = PfCfg;
+    using C = PfCfg<D_>;
     constexpr int D = C::D, RING = C::RING, BK = C::BK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -164,7 +172,8 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
     uint64_t *pready = sfull + 2;        // P'(j) written, S(j) read                       (8 softmax warps)
     uint64_t *odone = pready + 1;        // O += P'(j) V(j) done                           (tensor core)
     uint64_t *qready = odone + 1;        // Q in tensor memory                             (4 softmax warps)
-    static_assert(3 * C::RING + 5 == C::NBAR, "barrier count");
+    uint64_t *ofinal = qready + 1;       // the last O update done (once per CTA)          (tensor core)
+    static_assert(3 * C::RING + 6 == C::NBAR, "barrier count");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.num_q_heads;
@@ -181,6 +190,7 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
         mbar_init(pready, 8);
         mbar_init(odone, 1);
         mbar_init(qready, 4);
+        mbar_init(ofinal, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -294,13 +304,13 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
         // score into the log2 domain, bg = kBias * sum_d Q~ * g takes the K codes' bias off
         float g, bg;
         {
-            uint4 qv[16];
+            uint4 qv[D / 8];
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
+            for (int c = 0; c < D / 8; ++c)
                 qv[c] = rvalid ? __ldg(reinterpret_cast<const uint4 *>(a.q + qrow) + c) : make_uint4(0, 0, 0, 0);
             float mx = 0.f;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < D / 8; ++c) {
                 const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -316,7 +326,7 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             g = a.q_scale_log2 * exp2i(-e);
             float qsum = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            for (int half = 0; half < D / 64; ++half) {
                 uint32_t hq[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -435,7 +445,7 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
                         tc_fence_after();
                         const float of = resc ? factor : 1.f;
 #pragma unroll 1
-                        for (int q8 = 0; q8 < 8; ++q8) {
+                        for (int q8 = 0; q8 < D / 16; ++q8) {
                             uint32_t orr[16];
                             tmem_ld16(tmem + lane_base + C::O_COL + 16 * q8, orr);
                             tmem_wait_ld();
@@ -487,20 +497,20 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             if (lane == 0)
                 mbar_arrive(pready);
         }
-        // ---- epilogue: out = O / (sum of p * 2^(6-E)), half hf writing d = 64 hf .. 64 hf + 63
+        // ---- epilogue: out = O / (sum of p * 2^(6-E)), half hf writing d = D/2 hf .. D/2 hf + D/2 - 1
         if (j == nb) {
             float *ls2 = xm + (nb & 1) * 2 * C::M;  // parity slot the last block did not use
             ls2[hf * C::M + r] = lp;
             named_bar(C::BAR_SM, 256);
             const float lt = ls2[r] + ls2[C::M + r];
-            ok &= wait_phase(odone, (uint32_t)(nb - 1) & 1u, abort_flag);
+            ok &= wait_phase(ofinal, 0u, abort_flag);  // the CTA's last O update
             tc_fence_after();
             const float of = lt > 0.f ? 1.f / lt : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow + 64 * hf);
+            uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow + (D / 2) * hf);
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
+            for (int q2 = 0; q2 < D / 64; ++q2) {
                 uint32_t orr[32];
-                tmem_ld32(tmem + lane_base + C::O_COL + 64 * hf + 32 * q2, orr);
+                tmem_ld32(tmem + lane_base + C::O_COL + (D / 2) * hf + 32 * q2, orr);
                 tmem_wait_ld();
                 if (rvalid) {
 #pragma unroll
@@ -532,16 +542,16 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             uint8_t *st = base + C::OFF_RING + r * C::STAGE;
             const size_t rec = (size_t)b * a.tiles_max + (t_first + 2 * j + t - tf);  // < tiles_max (pf_seq_shape)
             if (lane < 2)
-                mbar_arrive_expect_tx(tfull + 2 * r + lane, kTileImg + kTileRec);
+                mbar_arrive_expect_tx(tfull + 2 * r + lane, C::IMG + kTileRec);
             __syncwarp();
             if (lane < 8) {
                 uint64_t *bar = tfull + 2 * r + t;
-                const uint8_t *img = a.img + rec * kTileImg;
+                const uint8_t *img = a.img + rec * C::IMG;
                 if (k == 0)
-                    bulk_load(st + C::ST_K + t * (kTileImg / 2), img, kTileImg / 2, bar);
+                    bulk_load(st + C::ST_K + t * (C::IMG / 2), img, C::IMG / 2, bar);
                 else if (k < 3)
-                    bulk_load(st + C::ST_V + (k - 1) * C::CODES + t * (kTileImg / 4), img + (kTileImg / 4) * (k + 1),
-                              kTileImg / 4, bar);
+                    bulk_load(st + C::ST_V + (k - 1) * C::CODES + t * (C::IMG / 4), img + (C::IMG / 4) * (k + 1),
+                              C::IMG / 4, bar);
                 else
                     bulk_load(st + C::ST_REC + t * kTileRec, a.srec + rec * kTileRec, kTileRec, bar);
             }
@@ -565,7 +575,7 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
             int n_s = 0, n_o = 0;
             // O += P'(k) V(k): P' from S buffer k & 1 (keys 16kk .. 16kk+15 at column
             // 64 (kk / 4) + 8 (kk % 4)), V (fp16 in ring stage k % RING) from shared memory;
-            // 16-key step kk = key groups 2kk, 2kk+1: half kk % 2 at 4096 (kk / 2)
+            // 16-key step kk = key groups 2kk, 2kk+1: half kk % 2 at V_W (kk / 2)
             auto issue_o = [&](int k) -> bool {
                 if (!wait_phase(pready, (uint32_t)k & 1u, abort_flag))
                     return false;
@@ -575,7 +585,7 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     umma_f16_ts(tmem + C::O_COL, tmem + pcol + 64 * (kk >> 2) + 8 * (kk & 3),
-                                desc_add(vd, (kk & 1) * C::CODES + (kk >> 1) * 4096), IDESC_O, k > 0 || kk > 0);
+                                desc_add(vd, (kk & 1) * C::CODES + (kk >> 1) * C::V_W), IDESC_O, k > 0 || kk > 0);
                 umma_commit(odone);
                 umma_commit(tfree + (k % RING));  // the stage's V is read: the TMA warp may refill it
                 ++n_o;
@@ -600,8 +610,8 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
                 if (j >= 1)
                     ok = issue_o(j - 1);
             }
-            if (ok && n_s == nb)
-                issue_o(nb - 1);
+            if (ok && n_s == nb && issue_o(nb - 1))
+                umma_commit(ofinal);
             if (*abort_flag) {
                 if (n_o > 0)
                     mbar_wait_drain(odone, (uint32_t)(n_o - 1) & 1u);
@@ -625,8 +635,10 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1) prefill_tc_kernel(const __g
 // and V scale 0, and record nt (past the sequence's last tile) is all such
 // keys.  Codes are converted exactly: K to code + 1152 (the exponent-bias
 // form of its byte; the attention kernel takes the bias off), V to the code.
+template <int D>
 __global__ void __launch_bounds__(256) kv_tile_images_kernel(const __grid_constant__ PrefillArgs a)
 {
+    using C = PfCfg<D>;
     griddep_wait();  // the appended keys are visible from here
     griddep_launch_dependents();
     const int b = blockIdx.y, idx = blockIdx.x, tid = threadIdx.x;
@@ -634,7 +646,7 @@ __global__ void __launch_bounds__(256) kv_tile_images_kernel(const __grid_consta
     if (!pf_seq_shape(a, b, L, q0, qlen, klo, tf, nt) || idx > nt)
         return;
     const int T = tf + idx;
-    uint8_t *img = a.img + ((size_t)b * a.tiles_max + idx) * kTileImg;
+    uint8_t *img = a.img + ((size_t)b * a.tiles_max + idx) * C::IMG;
     float *rec = reinterpret_cast<float *>(a.srec + ((size_t)b * a.tiles_max + idx) * kTileRec);
     __shared__ int s_row[kTileTokens];  // cache row of each key, -1 = not valid
     __shared__ float s_vmax[2];
@@ -670,66 +682,77 @@ __global__ void __launch_bounds__(256) kv_tile_images_kernel(const __grid_consta
         rec[2 * kTileTokens + 2] = 0.f;
         rec[2 * kTileTokens + 3] = 0.f;
     }
-    // K part: 16-byte piece at byte o holds key 8 (o / 2048) + (o / 16) % 8, d = 8 ((o / 128) % 16) ..
-    for (int c = tid; c < kTileImg / 32; c += 256) {
+    // K part: 16-byte piece at byte o holds key 8 (o / RS) + (o / 16) % 8, d = 8 ((o % RS) / 128) ..
+    for (int c = tid; c < C::IMG / 32; c += 256) {
         const uint32_t o = 16u * c;
-        const int key = (int)(o >> 11) * 8 + (int)((o >> 4) & 7);
-        const int d0 = (int)((o >> 7) & 15) * 8;
+        const int key = (int)(o / C::RS) * 8 + (int)((o >> 4) & 7);
+        const int d0 = (int)((o % C::RS) >> 7) * 8;
         const int row = s_row[key];
-        const uint2 w = row >= 0 ? __ldg(reinterpret_cast<const uint2 *>(a.k_codes + (size_t)row * kBlockD + d0))
+        const uint2 w = row >= 0 ? __ldg(reinterpret_cast<const uint2 *>(a.k_codes + (size_t)row * D + d0))
                                  : make_uint2(0u, 0u);
         const uint32_t t0 = w.x ^ 0x80808080u, t1 = w.y ^ 0x80808080u;
         *reinterpret_cast<uint4 *>(img + o) =
             make_uint4(__byte_perm(t0, 0x64646464u, 0x5140), __byte_perm(t0, 0x64646464u, 0x7362),
                        __byte_perm(t1, 0x64646464u, 0x5140), __byte_perm(t1, 0x64646464u, 0x7362));
     }
-    // V part: piece h (8 KB) holds the keys 32 w + 8 g + i with g / 2 == h, the 16-byte piece at
-    // byte o of it key 32 (o / 4096) + 8 (2 h + (o / 2048) % 2) + (o / 16) % 8, d = 8 ((o / 128) % 16) ..
-    for (int c = tid; c < kTileImg / 32; c += 256) {
+    // V part: piece h (64 D bytes) holds the keys 32 w + 8 g + i with g / 2 == h, the 16-byte piece
+    // at byte p of it key 32 (p / V_W) + 8 (2 h + (p / RS) % 2) + (p / 16) % 8, d = 8 ((p % RS) / 128) ..
+    for (int c = tid; c < C::IMG / 32; c += 256) {
         const uint32_t o = 16u * c;
-        const int h = (int)(o >> 13);
-        const uint32_t p = o & 8191u;
-        const int key = (int)(p >> 12) * 32 + (2 * h + (int)((p >> 11) & 1)) * 8 + (int)((p >> 4) & 7);
-        const int d0 = (int)((p >> 7) & 15) * 8;
+        const int h = (int)(o / (C::IMG / 4));
+        const uint32_t p = o % (C::IMG / 4);
+        const int key = (int)(p / C::V_W) * 32 + (2 * h + (int)((p / C::RS) & 1)) * 8 + (int)((p >> 4) & 7);
+        const int d0 = (int)((p % C::RS) >> 7) * 8;
         const int row = s_row[key];
-        const uint2 w = row >= 0 ? __ldg(reinterpret_cast<const uint2 *>(a.v_codes + (size_t)row * kBlockD + d0))
+        const uint2 w = row >= 0 ? __ldg(reinterpret_cast<const uint2 *>(a.v_codes + (size_t)row * D + d0))
                                  : make_uint2(0u, 0u);
         uint32_t v[4];
         i8x4_to_f16x2x2(w.x, v[0], v[1]);
         i8x4_to_f16x2x2(w.y, v[2], v[3]);
-        *reinterpret_cast<uint4 *>(img + kTileImg / 2 + o) = make_uint4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<uint4 *>(img + C::IMG / 2 + o) = make_uint4(v[0], v[1], v[2], v[3]);
     }
 }
 
-cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s)
+namespace {
+
+template <int D>
+cudaError_t launch_prefill_tc_t(const PrefillArgs &a, cudaStream_t s)
 {
+    using C = PfCfg<D>;
     static std::atomic<int> attr_set{0};
     if (!attr_set.load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             PfCfg::SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
         // the kernel moves registers between its warpgroups (setmaxnreg): the split must fit the
         // registers it is launched with, or a group would wait for registers forever
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
+        e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>);
         if (e != cudaSuccess)
             return e;
-        if (fa.numRegs != PfCfg::REG_LAUNCH)
+        if (fa.numRegs != C::REG_LAUNCH)
             return cudaErrorInvalidConfiguration;
         attr_set.store(1, std::memory_order_release);
     }
     // an upper bound of the tiles (sum over sequences of ceil(q_len / tpc)); CTAs past the
     // last tile leave at once
-    const int tpc = PfCfg::M / a.num_q_heads;
+    const int tpc = C::M / a.num_q_heads;
     const long long tiles = ((long long)a.total_q + tpc - 1) / tpc + a.batch;
     if (tiles > 0x7fffffffll)
         return cudaErrorInvalidConfiguration;
-    cudaError_t e = launch_pdl(kv_tile_images_kernel, dim3((unsigned)a.tiles_max, (unsigned)a.batch, 1), dim3(256),
-                               0, s, a);
+    cudaError_t e = launch_pdl(kv_tile_images_kernel<D>, dim3((unsigned)a.tiles_max, (unsigned)a.batch, 1),
+                               dim3(256), 0, s, a);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(prefill_tc_kernel, dim3((unsigned)tiles, 1, 1), dim3(PfCfg::THREADS), PfCfg::SMEM_BYTES, s, a);
+    return launch_pdl(prefill_tc_kernel<D>, dim3((unsigned)tiles, 1, 1), dim3(C::THREADS), C::SMEM_BYTES, s, a);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, int head_dim, cudaStream_t s)
+{
+    return head_dim == 64 ? launch_prefill_tc_t<64>(a, s) : launch_prefill_tc_t<128>(a, s);
 }
 
 // Tile records per sequence a prefill of this shape needs (its tiles plus the all-invalid one):
@@ -744,7 +767,7 @@ int prefill_tiles_max(int max_seq_len, int window, int max_q_len)
     return (int)(t + 1);
 }
 
-size_t prefill_tile_image_bytes() { return kTileImg; }
+size_t prefill_tile_image_bytes(int head_dim) { return head_dim == 64 ? tile_img_bytes<64>() : tile_img_bytes<128>(); }
 size_t prefill_tile_record_bytes() { return kTileRec; }
 
 }  // namespace mqa

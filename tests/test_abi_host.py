@@ -148,26 +148,32 @@ def test_combine_and_prefill_validation(L):
     assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), FAKE, 5, 65, FAKE, FAKE, 8, 0.1, None, 0, None, None) == mk.MQA_ERR_INVALID_ARG
     assert P(arr, 1, lm, 1, 0, -3, ctypes.byref(b), FAKE, 5, 3, FAKE, FAKE, 8, 0.1, None, 0, None, None) == mk.MQA_ERR_INVALID_ARG
     assert P(arr, 1, lm, 1, 0, 0, ctypes.byref(b), FAKE, 5, 3, FAKE, FAKE, 24, 0.1, None, 0, None, None) == mk.MQA_ERR_UNSUPPORTED
-    # head_dim 128 converts the key tiles into a workspace first: missing or short -> rejected
+    # the key tiles are converted into a workspace first: missing or short -> rejected
     arr128 = (mk._Cache * 1)(cache(d=128, page=64))
     b128, k128 = batch(max_blocks=4, max_seq_len=256, lens=[200, 130])
     need = mk.mqa_prefill_workspace_size(2, 256, 0, 3, 128)
-    assert need > 0 and mk.mqa_prefill_workspace_size(2, 256, 0, 3, 64) == 0
+    assert need > 0 and mk.mqa_prefill_workspace_size(2, 256, 0, 3, 96) == 0
     assert P(arr128, 1, lm, 1, 0, 0, ctypes.byref(b128), FAKE, 5, 3, FAKE, FAKE, 32, 0.1, None, 0, None,
              None) == mk.MQA_ERR_WORKSPACE
     assert P(arr128, 1, lm, 1, 0, 0, ctypes.byref(b128), FAKE, 5, 3, FAKE, FAKE, 32, 0.1, FAKE, need - 1, None,
+             None) == mk.MQA_ERR_WORKSPACE
+    arr64 = (mk._Cache * 1)(cache(d=64, page=16))
+    b64, k64 = batch(max_blocks=16, max_seq_len=256, lens=[200, 130])
+    assert P(arr64, 1, lm, 1, 0, 0, ctypes.byref(b64), FAKE, 5, 3, FAKE, FAKE, 8, 0.1, None, 0, None,
              None) == mk.MQA_ERR_WORKSPACE
 
 
 def test_prefill_workspace_formula(L):
     r256 = lambda x: (x + 255) // 256 * 256
-    # per sequence: the tiles of the key range plus one all-invalid tile; 32 KiB images, 528-byte records
+    # per sequence: the tiles of the key range plus one all-invalid tile; 256 * head_dim byte images,
+    # 528-byte records
     for B, Lmax, W, Q in ((3, 8704, 0, 512), (256, 8704, 1024, 512), (5, 100, 1024, 7), (2, 64, 0, 64)):
         tiles = -(-Lmax // 64)
         if W > 0:
             tiles = min(tiles, (W + Q - 2) // 64 + 2)
         n = B * (tiles + 1)
-        assert mk.mqa_prefill_workspace_size(B, Lmax, W, Q, 128) == r256(n * 32768) + n * 528
+        for d in (64, 128):
+            assert mk.mqa_prefill_workspace_size(B, Lmax, W, Q, d) == r256(n * 256 * d) + n * 528
 
 
 def test_auto_splits_validation(L):
