@@ -193,17 +193,6 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         : "memory");
 }
 
-// ---------------------------------------------------------------- warp MMA
-// D = A * B + D with A 16x16 (row), B 16x8 (col), fp16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // ---------------------------------------------------------------- int8 -> fp16
 // Exponent-bias ("magic number") conversion, as described for int8 weights in
 // Kim et al., "Who Says Elephants Can't Run: Bringing Large Scale MoE Models
@@ -223,18 +212,6 @@ __device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32
     const uint32_t t = w ^ 0x80808080u;
     lo = hsub2_1152(__byte_perm(t, 0x64646464u, 0x5140));
     hi = hsub2_1152(__byte_perm(t, 0x64646464u, 0x7362));
-}
-
-// Two words of four codes (a = token A, b = token B, byte i = column i) ->
-// four f16x2 values {A_i, B_i} for i = 0..3.
-__device__ __forceinline__ void i8x4x2_interleave_to_f16x2(uint32_t a, uint32_t b, uint32_t (&r)[4])
-{
-    const uint32_t t0 = __byte_perm(a, b, 0x5140) ^ 0x80808080u;  // A0 B0 A1 B1
-    const uint32_t t1 = __byte_perm(a, b, 0x7362) ^ 0x80808080u;  // A2 B2 A3 B3
-    r[0] = hsub2_1152(__byte_perm(t0, 0x64646464u, 0x5140));
-    r[1] = hsub2_1152(__byte_perm(t0, 0x64646464u, 0x7362));
-    r[2] = hsub2_1152(__byte_perm(t1, 0x64646464u, 0x5140));
-    r[3] = hsub2_1152(__byte_perm(t1, 0x64646464u, 0x7362));
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
