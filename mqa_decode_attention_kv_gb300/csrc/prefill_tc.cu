@@ -26,25 +26,25 @@
 //                        ring stage (B).
 // Scores and O accumulate in fp32 tensor memory.
 //
-// Roles (16 warps, one CTA per SM):
-//   warps 0-7   softmax, two warpgroups: half hf takes keys 64 hf .. 64 hf + 63
-//               of every block, thread r of each half owns query row r
-//               (tensor-memory lane r).  Half 0 converts the row of Q to fp16
+// Roles (20 warps, one CTA per SM):
+//   warps 0-15  softmax, four warpgroups: quarter q takes keys 32 q .. 32 q + 31
+//               of every block, thread r of each quarter owns query row r
+//               (tensor-memory lane r).  Quarter 0 converts the row of Q to fp16
 //               times one exact power of two into tensor memory.  Per block a
-//               thread reads its 64 scores, takes off the K codes' exponent
+//               thread reads its 32 scores, takes off the K codes' exponent
 //               bias (kBias * sum_d Q~[r][d]), applies the K scales and the
 //               row's causal / window mask and writes P' for its keys.  The
 //               row keeps one reference maximum (moved only when a score
-//               passes it by more than 2^8; the halves agree through a
+//               passes it by more than 2^8; the quarters agree through a
 //               barrier that ORs the need) and one power-of-two bound 2^E of
-//               the V scales.  At the end each half normalises its 64 columns
-//               of the row of O.
-//   warp 8      lane 0 issues every tcgen05.mma and commit, S(j) one block
+//               the V scales.  At the end each quarter normalises its D / 4
+//               columns of the row of O.
+//   warp 16     lane 0 issues every tcgen05.mma and commit, S(j) one block
 //               ahead of O += P'(j-1) V(j-1); the warp owns the tensor memory.
-//   warp 9      bulk copies: the two tile images and records of each block
+//   warp 17     bulk copies: the two tile images and records of each block
 //               into a ring stage once the O update that read the stage's
 //               previous block has completed.
-//   warps 10-11 idle (their registers go to the softmax warps).
+//   warps 18-19 idle (their registers go to the softmax warps).
 //
 // Every wait is bounded: a wait that runs out raises a CTA abort flag, every
 // role leaves at its next check (the softmax warps all together, at the
@@ -81,12 +81,13 @@ struct PfCfg {
     static constexpr int M = 128;                // query rows per CTA
     static constexpr int BK = kBlockTokens;      // keys per block
     static constexpr int RING = D == 64 ? 4 : 3;  // (head_dim 64: also keeps one CTA per SM)
-    static constexpr int THREADS = 384;
-    static constexpr int MMA_WARP = 8, TMA_WARP = 9;
+    static constexpr int QT = 4;                 // softmax warpgroups: each takes a quarter of a block's keys
+    static constexpr int THREADS = 128 * QT + 128;
+    static constexpr int MMA_WARP = 4 * QT, TMA_WARP = 4 * QT + 1;
     static constexpr int BAR_SM = 1;  // named barrier of the two softmax warpgroups
     static constexpr int REG_LAUNCH = (65536 / THREADS) / 8 * 8;  // 168
     static constexpr int REG_CTRL = 56;
-    static constexpr int REG_WORK = ((REG_LAUNCH * THREADS - 128 * REG_CTRL) / 256) / 8 * 8;
+    static constexpr int REG_WORK = ((REG_LAUNCH * THREADS - 128 * REG_CTRL) / (128 * QT)) / 8 * 8;
     static constexpr int CODES = BK * D;  // bytes of one V half (see the V layout below)
     static constexpr int V_W = 2 * RS;    // bytes of a 32-key group inside a V half
     // a ring stage: fp16 K of the block (its two tile images' K parts), fp16 V (their V
@@ -95,8 +96,9 @@ struct PfCfg {
     static constexpr int STAGE = (ST_REC + 2 * kTileRec + 1023) / 1024 * 1024;
     // shared memory
     static constexpr int OFF_RING = 0;
-    static constexpr int OFF_XM = OFF_RING + RING * STAGE;        // [2 parity][2 halves][128] row maxima / sums
-    static constexpr int OFF_MISC = OFF_XM + 2 * 2 * M * 4;       // tmem base, abort flag
+    static constexpr int OFF_XM = OFF_RING + RING * STAGE;        // [2 parity][QT][128] row maxima / sums
+    static constexpr int OFF_QG = OFF_XM + 2 * QT * M * 4;        // [2][128] g, bg of every row (quarter 0)
+    static constexpr int OFF_MISC = OFF_QG + 2 * M * 4;           // tmem base, abort flag
     static constexpr int OFF_MBAR = OFF_MISC + 64;
     static constexpr int NBAR = 3 * RING + 6;
     static constexpr int SMEM_BYTES = OFF_MBAR + 8 * NBAR + 1024;
@@ -118,7 +120,7 @@ struct PfCfg {
                       OFF_MBAR % 8 == 0,
                   "16-byte alignment");
     static_assert(O_COL + D <= S_COL && S_COL + 2 * 128 <= TMEM_COLS && Q_COL + D / 2 <= O_COL, "tensor memory");
-    static_assert(128 * (2 * REG_WORK + REG_CTRL) <= REG_LAUNCH * THREADS && REG_WORK >= REG_LAUNCH,
+    static_assert(128 * (QT * REG_WORK + REG_CTRL) <= REG_LAUNCH * THREADS && REG_WORK >= REG_LAUNCH,
                   "register split within the launch allocation");
 };
 
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
     uint64_t *tfull = reinterpret_cast<uint64_t *>(base + C::OFF_MBAR);  // [RING][2] tile images landed (copies)
     uint64_t *tfree = tfull + 2 * RING;  // [RING] stage free: O update of its block done (tensor core)
     uint64_t *sfull = tfree + RING;      // [2] S(j) done                                   (tensor core)
-    uint64_t *pready = sfull + 2;        // P'(j) written, S(j) read                       (8 softmax warps)
+    uint64_t *pready = sfull + 2;        // P'(j) written, S(j) read                       (16 softmax warps)
     uint64_t *odone = pready + 1;        // O += P'(j) V(j) done                           (tensor core)
     uint64_t *qready = odone + 1;        // Q in tensor memory                             (4 softmax warps)
     uint64_t *ofinal = qready + 1;       // the last O update done (once per CTA)          (tensor core)
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
             mbar_init(tfree + s, 1);
         for (int s = 0; s < 2; ++s)
             mbar_init(sfull + s, 1);
-        mbar_init(pready, 8);
+        mbar_init(pready, 4 * C::QT);
         mbar_init(odone, 1);
         mbar_init(qready, 4);
         mbar_init(ofinal, 1);
@@ -287,11 +289,11 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
 
     if (warp < C::MMA_WARP) {
         // ================================================================ softmax
-        // two warpgroups: half hf takes keys 64 hf .. 64 hf + 63 of every block for all 128
-        // rows; thread r of each half owns query row r (tensor-memory lane r).  Both halves keep
-        // the same reference per row; they agree on moving it through a barrier that ORs the
-        // need (rare), and half 0 rescales O.
-        const int hf = warp >> 2;
+        // four warpgroups: quarter qt takes keys 32 qt .. 32 qt + 31 of every block for all 128
+        // rows; thread r of each quarter owns query row r (tensor-memory lane r).  Every quarter
+        // keeps the same reference per row; they agree on moving it through a barrier that ORs
+        // the need (rare), and quarter 0 rescales O.
+        const int qt = warp >> 2;  // quarter: keys 32 qt .. 32 qt + 31 of every block
         const int r = 32 * (warp & 3) + lane;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int t = r / H;
@@ -299,19 +301,21 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
         const int ipos = i0 + t;
         const int lo_r = W > 0 ? max(0, ipos - W + 1) : 0;
         const size_t qrow = ((size_t)(q0 + t_begin) * H + r) * D;
-        float* xm = reinterpret_cast<float *>(base + C::OFF_XM);  // [2 parity][2 halves][128]
-        // ---- Q row: fp16 times 2^e (exact); half 0 writes it to tensor memory.  g turns a raw
+        float* xm = reinterpret_cast<float *>(base + C::OFF_XM);  // [2 parity][QT][128]
+        // ---- Q row: fp16 times 2^e (exact); quarter 0 writes it to tensor memory.  g turns a raw
         // score into the log2 domain, bg = kBias * sum_d Q~ * g takes the K codes' bias off
         float g, bg;
-        {
-            uint4 qv[D / 8];
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c)
-                qv[c] = rvalid ? __ldg(reinterpret_cast<const uint4 *>(a.q + qrow) + c) : make_uint4(0, 0, 0, 0);
+        float *qgb = reinterpret_cast<float *>(base + C::OFF_QG);
+        if (qt == 0) {
+            // quarter 0 converts the rows and publishes g, bg for the other quarters; two passes
+            // over the row (the second from L1): its largest magnitude, then the conversion 64 d
+            // at a time (the softmax threads run with ~100 registers)
+            const uint4 *qg = reinterpret_cast<const uint4 *>(a.q + qrow);
             float mx = 0.f;
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
-                const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+                const uint4 v = rvalid ? __ldg(qg + c) : make_uint4(0, 0, 0, 0);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[u] << 16)), fabsf(__uint_as_float(w4[u] & 0xffff0000u))));
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
                 uint32_t hq[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 v = qv[8 * half + c];
+                    const uint4 v = rvalid ? __ldg(qg + 8 * half + c) : make_uint4(0, 0, 0, 0);
                     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -340,21 +344,23 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
                         qsum += __high2float(h2);
                     }
                 }
-                if (hf == 0)
-                    tmem_st32(tmem + lane_base + C::Q_COL + 32 * half, hq);
+                tmem_st32(tmem + lane_base + C::Q_COL + 32 * half, hq);
             }
             bg = kBiasK * qsum * g;
-            if (hf == 0) {
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(qready);
-            }
+            qgb[r] = g;
+            qgb[C::M + r] = bg;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(qready);
         }
-        // the row's state, the same in both halves: reference m (log2 domain), V-scale bound 2^E,
+        named_bar(C::BAR_SM, 128 * C::QT);  // g, bg of every row published
+        g = qgb[r];
+        bg = qgb[C::M + r];
+        // the row's state, the same in every quarter: reference m (log2 domain), V-scale bound 2^E,
         // and c = 6 - E - m, which turns a masked score into the exponent of p * 2^(6-E);
-        // lp: this half's sum of p * 2^(6-E)
+        // lp: this quarter's sum of p * 2^(6-E)
         float m_run = -INFINITY, cexp = 0.f, lp = 0.f;
         int E_run = -100;
         bool ok = true;
@@ -366,31 +372,30 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
             ok &= wait_done(tfull + 2 * rs + 1, (uint32_t)(j / RING) & 1u, abort_flag);
             ok &= wait_done(sfull + b2, (uint32_t)(j >> 1) & 1u, abort_flag);
             tc_fence_after();
-            // this half's keys are the block's tile hf: its record
+            // this quarter's keys are half qt % 2 of the block's tile qt / 2: its record
             const uint8_t *recs = base + C::OFF_RING + rs * C::STAGE + C::ST_REC;
-            const float *ks = reinterpret_cast<const float *>(recs + hf * kTileRec);
+            const uint8_t *rec_t = recs + (qt >> 1) * kTileRec;
+            const float *ks = reinterpret_cast<const float *>(rec_t) + 32 * (qt & 1);
             const float *vs = ks + kTileTokens;
-            const int kb = (t_first + 2 * j) * kTileTokens + 64 * hf;  // first key of this half-block
-            // every row sees every key of the half-block, and every key is valid
-            const bool full = kb >= lo_max && kb + 63 <= i0 && reinterpret_cast<const int *>(ks)[2 * kTileTokens + 1] != 0 &&
-                              rvalid;
+            const int kb = (t_first + 2 * j) * kTileTokens + 32 * qt;  // first key of this quarter
+            // every row sees every key of the quarter, and every key of its tile is valid
+            const bool full = kb >= lo_max && kb + 31 <= i0 &&
+                              reinterpret_cast<const int *>(rec_t)[2 * kTileTokens + 1] != 0 && rvalid;
             // ---- exponent arguments y = x + c (x the masked log2-domain score, -inf when masked),
             // as fp32 pairs: y = ((S g - b g) k_s) + c
-            uint64_t y2[32];
+            uint64_t y2[16];
             float ymx[2] = {-INFINITY, -INFINITY};  // independent partial maxima
             {
-                uint32_t sr2[2][32];
-                tmem_ld32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 64 * hf, sr2[0]);
-                tmem_ld32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 64 * hf + 32, sr2[1]);
+                uint32_t sr[32];
+                tmem_ld32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 32 * qt, sr);
                 tmem_wait_ld();
                 const uint64_t g2 = f2pack(g, g), nbg2 = f2pack(-bg, -bg), c2 = f2pack(cexp, cexp);
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
+                {
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 k4 = reinterpret_cast<const float4 *>(ks)[8 * q2 + c4];
-                        const uint32_t *sv = &sr2[q2][4 * c4];
-                        const int c = 32 * q2 + 4 * c4;  // first key (of the half-block) of the four
+                        const float4 k4 = reinterpret_cast<const float4 *>(ks)[c4];
+                        const uint32_t *sv = &sr[4 * c4];
+                        const int c = 4 * c4;  // first key (of the quarter) of the four
                         uint64_t ya = fma2(fma2(f2pack(__uint_as_float(sv[0]), __uint_as_float(sv[1])), g2, nbg2),
                                            f2pack(k4.x, k4.y), c2);
                         uint64_t yb = fma2(fma2(f2pack(__uint_as_float(sv[2]), __uint_as_float(sv[3])), g2, nbg2),
@@ -422,21 +427,24 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
             const bool need = (m_run == -INFINITY && ymax != -INFINITY) || !(ymax <= 14.f - (float)E_run) ||
                               !(vmx <= exp2i(E_run));
             ok &= *abort_flag == 0;
-            if (named_bar_or(C::BAR_SM, 256, need || !ok)) {
-                if (named_bar_or(C::BAR_SM, 256, !ok))
-                    break;  // abort: both halves leave here together
-                // ---- rare: the row's reference and V bound move (both halves compute the same)
-                float *xmp = xm + b2 * 2 * C::M;
-                xmp[hf * C::M + r] = ymax - cexp;  // this half's largest masked score (log2 domain)
-                named_bar(C::BAR_SM, 256);
-                const float xmax = fmaxf(xmp[r], xmp[C::M + r]);
+            if (named_bar_or(C::BAR_SM, 128 * C::QT, need || !ok)) {
+                if (named_bar_or(C::BAR_SM, 128 * C::QT, !ok))
+                    break;  // abort: every quarter leaves here together
+                // ---- rare: the row's reference and V bound move (every quarter computes the same)
+                float *xmp = xm + b2 * C::QT * C::M;
+                xmp[qt * C::M + r] = ymax - cexp;  // this quarter's largest masked score (log2 domain)
+                named_bar(C::BAR_SM, 128 * C::QT);
+                float xmax = xmp[r];
+#pragma unroll
+                for (int u = 1; u < C::QT; ++u)
+                    xmax = fmaxf(xmax, xmp[u * C::M + r]);
                 const float m_new = fmaxf(m_run, xmax);
                 const int E_new = max(E_run, ceil_log2_pow(vmx));
                 const float c_new = m_new == -INFINITY ? 0.f : (float)(6 - E_new) - m_new;
                 // old terms in the new units: 2^(m - m') 2^(E - E')
                 const float factor = m_run == -INFINITY ? 0.f : fast_exp2((m_run - m_new) + (float)(E_run - E_new));
                 lp *= factor;
-                if (hf == 0) {
+                if (qt == 0) {
                     // O of the previous blocks (its last update done: waited here) to the new units
                     const bool resc = j >= 1 && m_run != -INFINITY && factor != 1.f;
                     if (__any_sync(0xffffffffu, resc)) {
@@ -459,19 +467,20 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
                 }
                 const uint64_t dc2 = f2pack(c_new - cexp, c_new - cexp);
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
+                for (int c = 0; c < 16; ++c)
                     y2[c] = add2(y2[c], dc2);
                 m_run = m_new;
                 E_run = E_new;
                 cexp = c_new;
             }
-            // ---- P' = 2^y * s_v (fp16) in place of this half's scores in S buffer b2 (the O update
-            // that read this buffer's previous P' was issued before S(j), which it holds now)
+            // ---- P' = 2^y * s_v (fp16) in place of this quarter's scores in S buffer b2, keys
+            // 2c, 2c + 1 of the quarter in its column c (the O update that read this buffer's
+            // previous P' was issued before S(j), which it holds now)
             const bool live = m_run != -INFINITY;
-            uint32_t pk[32];
+            uint32_t pk[16];
             uint64_t ls2 = 0;  // (0.f, 0.f): independent partial sums
 #pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4) {
+            for (int c4 = 0; c4 < 8; ++c4) {
                 const float4 v4 = reinterpret_cast<const float4 *>(vs)[c4];
                 float y0, y1, y2v, y3;
                 f2unpack(y2[2 * c4], y0, y1);
@@ -490,37 +499,41 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
                 f2unpack(ls2, la, lb);
                 lp += la + lb;
             }
-            tmem_st32(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 64 * hf, pk);
+            tmem_st16(tmem + lane_base + C::S_COL + (uint32_t)b2 * BK + 32 * qt, pk);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(pready);
         }
-        // ---- epilogue: out = O / (sum of p * 2^(6-E)), half hf writing d = D/2 hf .. D/2 hf + D/2 - 1
+        // ---- epilogue: out = O / (sum of p * 2^(6-E)), quarter qt writing d = D/4 qt .. D/4 qt + D/4 - 1
         if (j == nb) {
-            float *ls2 = xm + (nb & 1) * 2 * C::M;  // parity slot the last block did not use
-            ls2[hf * C::M + r] = lp;
-            named_bar(C::BAR_SM, 256);
-            const float lt = ls2[r] + ls2[C::M + r];
+            float *ls2 = xm + (nb & 1) * C::QT * C::M;  // parity slot the last block did not use
+            ls2[qt * C::M + r] = lp;
+            named_bar(C::BAR_SM, 128 * C::QT);
+            float lt = 0.f;
+#pragma unroll
+            for (int u = 0; u < C::QT; ++u)
+                lt += ls2[u * C::M + r];
             ok &= wait_phase(ofinal, 0u, abort_flag);  // the CTA's last O update
             tc_fence_after();
             const float of = lt > 0.f ? 1.f / lt : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow + (D / 2) * hf);
+            uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow + (D / 4) * qt);
+            constexpr int NC = D / 4;  // columns of this quarter: 32 or 16
+            uint32_t orr[NC];
+            if constexpr (NC == 32)
+                tmem_ld32(tmem + lane_base + C::O_COL + NC * qt, orr);
+            else
+                tmem_ld16(tmem + lane_base + C::O_COL + NC * qt, orr);
+            tmem_wait_ld();
+            if (rvalid) {
 #pragma unroll
-            for (int q2 = 0; q2 < D / 64; ++q2) {
-                uint32_t orr[32];
-                tmem_ld32(tmem + lane_base + C::O_COL + (D / 2) * hf + 32 * q2, orr);
-                tmem_wait_ld();
-                if (rvalid) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        dst[4 * q2 + c] = make_uint4(
-                            pack_bf16x2(__uint_as_float(orr[8 * c + 0]) * of, __uint_as_float(orr[8 * c + 1]) * of),
-                            pack_bf16x2(__uint_as_float(orr[8 * c + 2]) * of, __uint_as_float(orr[8 * c + 3]) * of),
-                            pack_bf16x2(__uint_as_float(orr[8 * c + 4]) * of, __uint_as_float(orr[8 * c + 5]) * of),
-                            pack_bf16x2(__uint_as_float(orr[8 * c + 6]) * of, __uint_as_float(orr[8 * c + 7]) * of));
-                }
+                for (int c = 0; c < NC / 8; ++c)
+                    dst[c] = make_uint4(
+                        pack_bf16x2(__uint_as_float(orr[8 * c + 0]) * of, __uint_as_float(orr[8 * c + 1]) * of),
+                        pack_bf16x2(__uint_as_float(orr[8 * c + 2]) * of, __uint_as_float(orr[8 * c + 3]) * of),
+                        pack_bf16x2(__uint_as_float(orr[8 * c + 4]) * of, __uint_as_float(orr[8 * c + 5]) * of),
+                        pack_bf16x2(__uint_as_float(orr[8 * c + 6]) * of, __uint_as_float(orr[8 * c + 7]) * of));
             }
         }
         tc_fence_before();
@@ -574,7 +587,7 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
             const uint64_t vdesc0 = umma_sdesc(smem_u32(base + C::OFF_RING + C::ST_V), C::V_SR, C::V_SC);
             int n_s = 0, n_o = 0;
             // O += P'(k) V(k): P' from S buffer k & 1 (keys 16kk .. 16kk+15 at column
-            // 64 (kk / 4) + 8 (kk % 4)), V (fp16 in ring stage k % RING) from shared memory;
+            // 32 (kk / 2) + 8 (kk % 2)), V (fp16 in ring stage k % RING) from shared memory;
             // 16-key step kk = key groups 2kk, 2kk+1: half kk % 2 at V_W (kk / 2)
             auto issue_o = [&](int k) -> bool {
                 if (!wait_phase(pready, (uint32_t)k & 1u, abort_flag))
@@ -584,7 +597,7 @@ __global__ void __launch_bounds__(PfCfg<D_>::THREADS, 1) prefill_tc_kernel(const
                 const uint32_t pcol = C::S_COL + (uint32_t)(k & 1) * BK;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_f16_ts(tmem + C::O_COL, tmem + pcol + 64 * (kk >> 2) + 8 * (kk & 3),
+                    umma_f16_ts(tmem + C::O_COL, tmem + pcol + 32 * (kk >> 1) + 8 * (kk & 1),
                                 desc_add(vd, (kk & 1) * C::CODES + (kk >> 1) * C::V_W), IDESC_O, k > 0 || kk > 0);
                 umma_commit(odone);
                 umma_commit(tfree + (k % RING));  // the stage's V is read: the TMA warp may refill it
