@@ -123,3 +123,59 @@ def test_mixed_decode_rows_and_prefill_chunks_one_launch(num_decode, chunks):
         od = mk.mqa_decode_attn(st.gpu_caches, [0], 0, window, st.batch, qd, sm_scale=sm_scale(d))
         torch.cuda.synchronize()
         assert_close(od[torch.from_numpy(dec).cuda()], ref[cu_q[dec]], f"decode kernel rows W={window}")
+
+
+def _prefill_vs_oracle(st, lens, q_lens, q_bits, window, d):
+    cu_q = synth.cu_from_counts(q_lens)
+    out = mk.mqa_prefill_attn(st.gpu_caches, [0], 0, window, st.batch, to_dev_i32(cu_q), to_dev_bf16(q_bits),
+                              int(np.max(q_lens)), sm_scale=sm_scale(d))
+    torch.cuda.synchronize()
+    rs, rp = oracle.prefill_rows(cu_q, lens)
+    ref, _ = oracle.attention(st.ora_caches[0], st.pb.block_table, lens, q_bits, rs, rp, window, sm_scale(d))
+    return out, ref
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_prefill_large_magnitudes_stay_finite(d):
+    """V scales far above fp16's range, tiny queries, and V magnitudes that grow
+    along the sequence (the power-of-two bound of the V scales moves block after
+    block): every intermediate stays finite and the rows match the oracle."""
+    rng = np.random.default_rng(51 + d)
+    page, H = 64, 32 if d == 128 else 8
+    lens = np.array([700, 1500, 130], np.int32)
+    q_lens = np.array([300, 129, 130], np.int64)
+    T = int(lens.sum())
+    k = rng.standard_normal((T, d), dtype=np.float32) * np.float32(3e5)
+    growth = np.exp(np.linspace(0.0, 12.0, T, dtype=np.float32))[:, None]
+    v = rng.standard_normal((T, d), dtype=np.float32) * np.float32(3e5) * growth
+    st = build_caches(rng, lens, page, d, 1, kv_bits=[(synth.f32_to_bf16_bits(k), synth.f32_to_bf16_bits(v))])
+    q = synth.bf16_normal(rng, (int(q_lens.sum()), H, d), 1e-5)
+    for window in (0, 256):
+        out, ref = _prefill_vs_oracle(st, lens, q_lens, q, window, d)
+        g = out.float().cpu().numpy()
+        assert np.all(np.isfinite(g))
+        scale = np.abs(ref).max()
+        rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+        assert rel <= 5e-3 and np.abs(g - ref).max() <= 1e-2 * scale, (window, rel)
+
+
+@pytest.mark.parametrize("k_offset", [1.0, 30.0])
+def test_prefill_one_signed_queries_and_skewed_keys(k_offset):
+    """Queries of one sign and keys whose codes sit near one end of the int8
+    range: the K images carry their codes' exponent bias, which the softmax
+    takes off in fp32, so this is where that correction is largest."""
+    rng = np.random.default_rng(61)
+    d, page, H = 128, 64, 32
+    lens = np.array([1, 129, 1500, 700], np.int32)
+    q_lens = np.array([1, 129, 200, 64], np.int64)
+    T = int(lens.sum())
+    k = rng.standard_normal((T, d), dtype=np.float32) * np.float32(0.1 * k_offset) + np.float32(k_offset)
+    v = rng.standard_normal((T, d), dtype=np.float32)
+    st = build_caches(rng, lens, page, d, 1, kv_bits=[(synth.f32_to_bf16_bits(k), synth.f32_to_bf16_bits(v))])
+    for sign in (1.0, -1.0):
+        qf = (np.abs(rng.standard_normal((int(q_lens.sum()), H, d), dtype=np.float32)) + np.float32(0.5)) * \
+            np.float32(sign * 2.0)
+        q = synth.f32_to_bf16_bits(qf)
+        for window in (0, 1024):
+            out, ref = _prefill_vs_oracle(st, lens, q_lens, q, window, d)
+            assert_close(out, ref, f"prefill one-signed q sign {sign} window {window} k_offset {k_offset}")
