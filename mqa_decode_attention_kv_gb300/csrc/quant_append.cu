@@ -18,30 +18,48 @@ __global__ void __launch_bounds__(256) quant_append_kernel(AppendArgs a)
     constexpr int kLanesPerVec = D / 8;               // 16 (d=128) or 8 (d=64)
     constexpr int kVecsPerWarp = 32 / kLanesPerVec;   // 2 or 4
     constexpr int kTokensPerWarp = kVecsPerWarp / 2;  // K and V of a token
-    griddep_wait();  // the previous kernel on the stream (which may read the slots written here) is done
-    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int vec = lane / kLanesPerVec;              // which vector of the warp
     const int sub = lane % kLanesPerVec;              // 16-byte slice of the vector
     const int token = warp * kTokensPerWarp + (vec >> 1);
     const bool is_v = (vec & 1) != 0;
+    const bool active = token < a.num_tokens;
+    // while the previous kernel may still run: warm L2 with what this token's lanes read next
+    // (hints only: every load below comes after griddep_wait and sees what that kernel writes).
+    // The guessed sequence b = token is the one-token-per-sequence append of a decode step.
+    if (active && sub == 0) {
+        const int g = min(token, a.batch - 1);
+        prefetch_l2(a.cu_new + token);
+        prefetch_l2(a.seq_lens + g);
+        prefetch_l2((is_v ? a.v_new : a.k_new) + (size_t)token * D);
+        const char *row = reinterpret_cast<const char *>(a.block_table + (size_t)g * a.max_blocks);
+        for (int off = 0; off < a.max_blocks * 4 && off < 16 * 128; off += 128)
+            prefetch_l2(row + off);
+    }
+    griddep_wait();  // the previous kernel on the stream (which may read the slots written here) is done
+    griddep_launch_dependents();
     if (warp * kTokensPerWarp >= a.num_tokens)
         return;
-    const bool active = token < a.num_tokens;
 
-    // sequence of this token: the b with cu_new[b] <= token < cu_new[b+1]
+    // sequence of this token: the b with cu_new[b] <= token < cu_new[b+1]; one new token per
+    // sequence (b = token) is tested first with two independent loads
     int b = 0;
     if (active) {
-        int lo = 0, hi = a.batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(a.cu_new + mid) <= token)
-                lo = mid;
-            else
-                hi = mid - 1;
+        const int g = min(token, a.batch - 1);
+        if (__ldg(a.cu_new + g) <= token && token < __ldg(a.cu_new + g + 1)) {
+            b = g;
+        } else {
+            int lo = 0, hi = a.batch - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(a.cu_new + mid) <= token)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            b = lo;
         }
-        b = lo;
     }
 
     // load 8 bf16 values
