@@ -1,7 +1,10 @@
-// Decode attention on the 5th-generation tensor cores (tcgen05), head_dim 128,
-// groups of 32 query heads: one persistent kernel with worker warpgroups.
+// Decode attention on the 5th-generation tensor cores (tcgen05): one persistent
+// kernel with worker warpgroups.  A key block is 128 rows of 128 code bytes
+// (tensor-memory lanes): 128 tokens at head_dim 128, 256 tokens at head_dim 64
+// (two tokens a row; see TcMode).  A head group is 32 query heads at head_dim
+// 128 (fewer heads leave zero-query columns) and 16 at head_dim 64.
 //
-// Work.  The call's (sequence b, head group g, 128-token key block) triples
+// Work.  The call's (sequence b, head group g, key block) triples
 // form one list, ordered by b, then g, then block.  In the balanced mode CTA c
 // of the first G' = min(G, N) CTAs takes the contiguous share
 // [c*N/G', (c+1)*N/G') of the N list entries (never empty), so every CTA
@@ -18,12 +21,12 @@
 //
 // Roles (12 warps, one CTA per SM):
 //   warps 0-7   two worker warpgroups.  Worker group w takes the CTA's blocks
-//               i with i % 2 == w, whole: thread t owns token row t (= tensor
+//               i with i % 2 == w, whole: thread t owns row t (= tensor
 //               memory lane t).  Per block it converts the K codes to fp16
 //               (kept with their exponent bias +1152) straight into its K
 //               buffer in tensor memory (the A operand of S^T = K Q^T), the V
 //               codes to fp16 in place in the ring stage (the A operand of
-//               O^T += V^T P'), then reads its token's 32 scores, takes the K
+//               O^T += V^T P'), then reads its row's 32 scores, takes the K
 //               bias off, applies the K scale and writes
 //               P' = 2^(score - ref) * s_v * 2^(6-E) (fp16) for the MMA.  Each
 //               group keeps its own per-head reference maxima (moved only when

@@ -64,8 +64,8 @@ def ring_setup(rng, lens, page, d, ring, max_chunk):
 
 
 DECODE_CASES = [
-    # heads, d, page, window: the tcgen05 kernel (64-token pages and 16-token
-    # pages) and the mma.sync kernel (d=64, and d=128 below 32 heads)
+    # heads, d, page, window: 64-token and 16-token pages, two-token rows (d=64)
+    # and zero-query columns (d=128 with 16 heads)
     (32, 128, 64, 1024),
     (32, 128, 16, 300),
     (8, 64, 16, 200),
