@@ -1,7 +1,8 @@
 // Device helpers shared by the kernels of libmqa_kv (sm_103a only).
 //
-// Inline PTX wrappers for mbarriers, TMA (cp.async.bulk / cp.async.bulk.tensor),
-// the legacy warp-level tensor-core MMA, and the int8 -> fp16 conversion.
+// Inline PTX wrappers for mbarriers, programmatic dependent launch, L2 prefetch
+// and TMA (cp.async.bulk / cp.async.bulk.tensor); the exact int8 -> fp16
+// conversion; power-of-two and exponential helpers.
 #pragma once
 
 #include <cuda.h>
@@ -117,24 +118,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.  Returns false
-// on timeout (the caller reports it and leaves); never spins forever.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity))
-                return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs)
-            return false;
-    }
-}
-
-// The same with the drain limit: a CTA that is leaving early waits this long for
-// its own asynchronous copies and MMAs before it gives up.
+// Wait for phase `parity` of `bar` with the drain limit: a CTA that is leaving early
+// waits this long for its own asynchronous copies and MMAs before it gives up.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity)
 {
     if (mbar_try_wait_hint(bar, parity, kDrainSuspendNs))

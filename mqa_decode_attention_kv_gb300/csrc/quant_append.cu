@@ -3,8 +3,9 @@
 //
 // One group of head_dim/8 lanes handles one vector (K or V of one token): each
 // lane loads 16 bytes (8 bf16), the group reduces max|x| with shuffles, and
-// each lane writes 8 codes (8 bytes).  Bit-exact with IEEE fp32 division and
-// round-half-even conversion (no fast-math anywhere in this file).
+// each lane writes 8 codes (8 bytes) with kv_quant8 (IEEE fp32 division and
+// round-half-even conversion; the decode kernel's fused append uses the same
+// functions, so both write the same bits).
 #include "common.cuh"
 #include "kv_stage.cuh"
 #include "launch.h"
@@ -68,12 +69,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(AppendArgs a)
     if (active)
         raw = __ldg(reinterpret_cast<const uint4 *>(src + (size_t)token * D) + sub);
     float x[8];
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+    bf16x8_to_f32(raw, x);
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -108,18 +104,9 @@ __global__ void __launch_bounds__(256) quant_append_kernel(AppendArgs a)
     }
     const size_t slot = (size_t)blk * a.page_size + (pos % a.page_size);
 
-    const float s = __fdiv_rn(amax, 127.0f);
-    uint32_t packed[2] = {0u, 0u};
-    if (s != 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int c = __float2int_rn(__fdiv_rn(x[i], s));
-            c = max(-127, min(127, c));
-            packed[i >> 2] |= (uint32_t)(c & 0xff) << (8 * (i & 3));
-        }
-    }
+    const float s = kv_quant_scale(amax);
     int8_t *codes = is_v ? a.v_codes : a.k_codes;
-    reinterpret_cast<uint2 *>(codes + slot * D)[sub] = make_uint2(packed[0], packed[1]);
+    reinterpret_cast<uint2 *>(codes + slot * D)[sub] = kv_quant8(x, s);
     if (sub == 0)
         (is_v ? a.v_scale : a.k_scale)[slot] = s;
 }
