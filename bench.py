@@ -321,7 +321,7 @@ def e2e_steps(stack: DecodeStack, steps, stream, graph: bool):
     attention calls, D2H of all outputs.  graph=True captures that whole
     sequence (copies included) once into a CUDA graph and replays it, as a
     serving loop would; graph=False issues it eagerly every step (the host's
-    call overhead then shows).  Returns (per-step ms, h2d, d2h bytes)."""
+    call overhead then shows).  Returns (per-step ms, h2d, d2h bytes, the copy groups)."""
     import torch
     mk = stack.mk
     w = stack.w
@@ -351,35 +351,50 @@ def e2e_steps(stack: DecodeStack, steps, stream, graph: bool):
                                out=out_dev[l], num_splits=stack.splits[l], workspace=stack.ws, stream=s)
         out_host.copy_(out_dev, non_blocking=True)
 
+    # copies on their own stream, overlapping the layers, in few large copies: the queries in
+    # growing groups of layers (1, 2, 4, ...; the first with the new K/V), each group arriving
+    # while earlier layers run; the outputs in shrinking groups (half the layers left, then
+    # half of the rest, ...), each leaving once its last layer is done, so only the last
+    # layer's output is copied after the step's last kernel
+    L = w.num_layers
+    in_groups, a, n = [], 0, 1
+    while a < L:
+        in_groups.append((a, min(L, a + n)))
+        a, n = in_groups[-1][1], 2 * n
+    out_groups, a = [], 0
+    while a < L:
+        out_groups.append((a, a + (L - a + 1) // 2))
+        a = out_groups[-1][1]
+    out_after = {b - 1: (a, b) for a, b in out_groups}
+
     def one_step(s):
-        # copies on their own stream, overlapping the layers: layer l's queries arrive while
-        # earlier layers run, its output leaves while later layers run
         cs = copy_stream
         cs.wait_stream(s)
+        arrived = {}
         with torch.cuda.stream(cs):
-            kn_dev.copy_(kn_host, non_blocking=True)
-            vn_dev.copy_(vn_host, non_blocking=True)
-            kv_in = torch.cuda.Event()
-            kv_in.record(cs)
-            q_in = []
-            for l in range(w.num_layers):
-                q_dev[l].copy_(q_host[l], non_blocking=True)
-                q_in.append(torch.cuda.Event())
-                q_in[-1].record(cs)
-        s.wait_event(kv_in)
-        for l in range(w.num_layers):
-            s.wait_event(q_in[l])
+            for gi, (a, b) in enumerate(in_groups):
+                if gi == 0:
+                    kn_dev.copy_(kn_host, non_blocking=True)
+                    vn_dev.copy_(vn_host, non_blocking=True)
+                q_dev[a:b].copy_(q_host[a:b], non_blocking=True)
+                arrived[a] = torch.cuda.Event()
+                arrived[a].record(cs)
+        for l in range(L):
+            if l in arrived:
+                s.wait_event(arrived[l])
             c = stack.append_before.get(l)
             if c is not None:
                 mk.kv_quant_append(stack.caches[c], stack.batch_of_cache(c), stack.cu_step, w.batch, kn_dev[c],
                                    vn_dev[c], stream=s)
             mk.mqa_decode_attn(stack.caches, list(w.layer_map), l, w.windows[l], stack.batch_of_layer(l), q_dev[l],
                                out=out_dev[l], num_splits=stack.splits[l], workspace=stack.ws, stream=s)
-            done = torch.cuda.Event()
-            done.record(s)
-            cs.wait_event(done)
-            with torch.cuda.stream(cs):
-                out_host[l].copy_(out_dev[l], non_blocking=True)
+            if l in out_after:
+                a, b = out_after[l]
+                done = torch.cuda.Event()
+                done.record(s)
+                cs.wait_event(done)
+                with torch.cuda.stream(cs):
+                    out_host[a:b].copy_(out_dev[a:b], non_blocking=True)
         s.wait_stream(cs)
 
     run = None
@@ -403,7 +418,9 @@ def e2e_steps(stack: DecodeStack, steps, stream, graph: bool):
             e1.record(stream)
             times.append((e0, e1))
     stream.synchronize()
-    return [a.elapsed_time(b) for a, b in times], h2d, d2h
+    groups = "queries in groups of %s layers, outputs in groups of %s" % (
+        ", ".join(str(b - a) for a, b in in_groups), ", ".join(str(b - a) for a, b in out_groups))
+    return [a.elapsed_time(b) for a, b in times], h2d, d2h, groups
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
@@ -663,13 +680,13 @@ def run_decode(args, w):
     e2e = None
     if not args.no_e2e:
         n_e2e = max(3, min(args.steps, 10))
-        et, h2d, d2h = e2e_steps(stack, n_e2e, stream, graph=True)
-        ee, _, _ = e2e_steps(stack, n_e2e, stream, graph=False)
+        et, h2d, d2h, groups = e2e_steps(stack, n_e2e, stream, graph=True)
+        ee, _, _, _ = e2e_steps(stack, n_e2e, stream, graph=False)
         e2e = {"value": world * B / (statistics.mean(et) / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(et),
                "how": "public Python API, pinned host buffers; the step (H2D copies of every query and new "
                       "K/V, 12 appends, 24 decode calls, D2H of every output; copies on a second stream "
-                      "overlapping the layers) captured once into a CUDA graph and replayed",
+                      "overlapping the layers: " + groups + ") captured once into a CUDA graph and replayed",
                "eager": {"value": world * B / (statistics.mean(ee) / 1000.0), "ms_per_step": statistics.mean(ee),
                          "how": "the same calls issued eagerly every step, copies in line with the layers "
                                 "(three H2D copies before, one D2H after)"}}
