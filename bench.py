@@ -418,6 +418,10 @@ def e2e_steps(stack: DecodeStack, steps, stream, graph: bool):
             e1.record(stream)
             times.append((e0, e1))
     stream.synchronize()
+    # the outputs that reached the host are the device path's, bit for bit (the kernels are
+    # deterministic and every step appends the same tokens): a copy that went wrong fails here
+    if not torch.equal(out_host.view(torch.int16), stack.out.cpu().view(torch.int16)):
+        raise SystemExit("end-to-end outputs differ from the device path's")
     groups = "queries in groups of %s layers, outputs in groups of %s" % (
         ", ".join(str(b - a) for a, b in in_groups), ", ".join(str(b - a) for a, b in out_groups))
     return [a.elapsed_time(b) for a, b in times], h2d, d2h, groups
